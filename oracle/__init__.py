@@ -1,0 +1,139 @@
+"""Oracle for the TREDUCE / window-collective hot path (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package. The
+product path (``tile_level_collective_gb300``) never imports it and shares no
+code with it.
+
+The arithmetic lives in ``oracle.c`` (plain single-threaded C, compiled with
+``-ffp-contract=off`` and no fast-math). This module only builds that file with
+gcc, loads it and passes numpy buffers to it. Element types are given as the
+oracle's own codes below; 16-bit floating types travel as ``uint16`` arrays
+holding the raw encodings.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+# ReduceOp values (TREDUCE article, section 1.3).
+SUM, MAX, MIN = 0, 1, 2
+# The oracle's element-type codes.
+F32, F16, BF16, I32 = 0, 1, 2, 3
+ELEM_BYTES = {F32: 4, F16: 2, BF16: 2, I32: 4}
+NUMPY_TYPE = {F32: np.float32, F16: np.uint16, BF16: np.uint16, I32: np.int32}
+
+_lib = None
+
+
+def build(force=False):
+    """Compile oracle.c into liboracle.so beside it (gcc, plain flags)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.check_call(cmd)
+        os.replace(tmp, _LIB)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.oracle_treduce.argtypes = [ctypes.POINTER(vp), i32, i32, vp, i64, i64, i64, i32, i32]
+        L.oracle_reduce_scatter.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
+        L.oracle_allgather.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32]
+        L.oracle_all_to_all_v.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                          ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                          i32, i64, i64, i32]
+        for name in ("oracle_treduce", "oracle_reduce_scatter", "oracle_allgather",
+                     "oracle_all_to_all_v"):
+            getattr(L, name).restype = ctypes.c_int
+        L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        L.oracle_f32_to_f16.restype = ctypes.c_uint16
+        L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_bf16_to_f32.restype = ctypes.c_float
+        L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.oracle_f16_to_f32.restype = ctypes.c_float
+        for name in ("oracle_f32_to_bf16_array", "oracle_f32_to_f16_array",
+                     "oracle_f16_to_f32_array", "oracle_bf16_to_f32_array"):
+            getattr(L, name).argtypes = [vp, vp, i64]
+            getattr(L, name).restype = None
+        _lib = L
+    return _lib
+
+
+def _ptrs(arrays):
+    for a in arrays:
+        if not a.flags.c_contiguous:
+            raise ValueError("oracle buffers must be C-contiguous")
+    return (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+
+
+def treduce(srcs, dst, valid_rows, valid_cols, ld, op, dtype, root=0):
+    """dst[i*ld+j] = reduction over srcs in the page's rank order; see oracle.c."""
+    return lib().oracle_treduce(_ptrs(srcs), len(srcs), root, dst.ctypes.data,
+                                valid_rows, valid_cols, ld, op, dtype)
+
+
+def reduce_scatter(windows, rows, cols, ld, op, dtype):
+    return lib().oracle_reduce_scatter(_ptrs(windows), len(windows), rows, cols, ld, op, dtype)
+
+
+def allgather(windows, rows, cols, ld, dtype):
+    return lib().oracle_allgather(_ptrs(windows), len(windows), rows, cols, ld, dtype)
+
+
+def all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows, size, elem_size):
+    n = len(inputs)
+    assert len(targets) == n and len(send_counts) == n and len(recv_counts) == n
+    for c in list(send_counts) + list(recv_counts):
+        assert c.dtype == np.int32
+    return lib().oracle_all_to_all_v(_ptrs(inputs), _ptrs(targets), _ptrs(send_counts),
+                                     _ptrs(recv_counts), n, target_rows, size, elem_size)
+
+
+def f32_to_bf16(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_f32_to_bf16_array(x.ctypes.data, y.ctypes.data, x.size)
+    return y
+
+
+def f32_to_f16(x):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_f32_to_f16_array(x.ctypes.data, y.ctypes.data, x.size)
+    return y
+
+
+def f16_to_f32(h):
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    y = np.empty(h.shape, dtype=np.float32)
+    lib().oracle_f16_to_f32_array(h.ctypes.data, y.ctypes.data, h.size)
+    return y
+
+
+def bf16_to_f32(h):
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    y = np.empty(h.shape, dtype=np.float32)
+    lib().oracle_bf16_to_f32_array(h.ctypes.data, y.ctypes.data, h.size)
+    return y
