@@ -1,0 +1,650 @@
+"""Benchmark of the TREDUCE / window-collective hot path on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Default workload: TREDUCE over 8 ranks of bf16 [4096, 4096] with a 4000 x 4000
+valid box inside NaN-sentinel padding, N(0, 1) values; one step = Sum, Max and
+Min (three launches). Metric: effective HBM GB/s = (N + 1) * bytes/elem *
+valid elements per launch, summed over the step, divided by the step's device
+time. Inputs are generated on the host by the seeded generator and resident in
+HBM before timing; L2 is flushed (a 256 MiB write, outside the timed events)
+before every step. Other workloads (the parity configurations) can be timed
+with --workload for the per-kernel evidence.
+
+--impl reference times the CPU oracle on this machine's host cores (the only
+other implementation there is), on a bounded sample of the same workload per
+step. Multi-GPU (torchrun): every rank runs an independent replica (the path
+has no cross-GPU exchange); value is the total over ranks / max time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TREDUCE effective HBM GB/s (N reads + 1 write) and % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["tile_level_collective_gb300/csrc/reduce_impl.cuh",
+                  "tile_level_collective_gb300/csrc/movement.cu",
+                  "tile_level_collective_gb300/csrc/ptoc_api.cu",
+                  "tile_level_collective_gb300/csrc/ptoc_internal.h"]
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Workload:
+    """One benchmark workload: host inputs, device buffers, the launches of a
+    step and its algorithmic bytes."""
+    name = ""
+    dtype_compute = "f32"
+    storage = ""
+    kernel = ""
+
+    def config(self):
+        raise NotImplementedError
+
+
+class TreduceBench(Workload):
+    def __init__(self, w, storage):
+        self.w, self.storage = w, storage
+        self.name = w.name
+        self.kernel = "reduce_kernel (%s)" % storage
+        self.dtype_compute = "i32" if storage == "i32" else "f32"
+
+    def bytes_per_launch(self):
+        return self.w.algorithmic_bytes()
+
+    def launches_per_step(self):
+        return len(self.w.ops)
+
+    def bytes_per_step(self):
+        return self.bytes_per_launch() * self.launches_per_step()
+
+    def setup_host(self):
+        import numpy as np
+        self.host = [np.ascontiguousarray(self.w.slice(r)) for r in range(self.w.nranks)]
+
+    def setup_device(self, dev):
+        import numpy as np
+        import torch
+        w = self.w
+        self.dev = [_to_dev(h, dev) for h in self.host]
+        pad = w.dst_pad if w.dst_pad is not None else 0
+        self.dst_init = np.empty((w.rows, w.ld), dtype=self.host[0].dtype)
+        self.dst_init.view(np.uint16 if self.dst_init.itemsize == 2 else np.uint32)[...] = pad
+        self.dsts = [_to_dev(self.dst_init, dev) for _ in w.ops]
+
+    def launch(self, i, srcs=None, dst=None):
+        import tile_level_collective_gb300 as P
+        w = self.w
+        code = {"f32": P.F32, "f16": P.F16, "bf16": P.BF16, "i32": P.I32}[self.storage]
+        P.ptoc_treduce(srcs or self.dev, dst if dst is not None else self.dsts[i], w.rows, w.cols,
+                       w.valid_rows, w.valid_cols, w.ld, P.OPS[w.ops[i]], code)
+
+    # e2e: inputs copied from pinned host memory each step, results read back
+    def setup_e2e(self, dev):
+        import torch
+        self.pinned = [_pin(h) for h in self.host]
+        self.out_pinned = [torch.empty(_nbytes(self.dst_init), dtype=torch.uint8).pin_memory()
+                           for _ in self.w.ops]
+        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+
+    def e2e_step(self):
+        for d, h in zip(self.e2e_dev, self.pinned):
+            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+        for i in range(self.launches_per_step()):
+            self.launch(i, srcs=self.e2e_dev)
+        for i, o in enumerate(self.out_pinned):
+            o.copy_(self.dsts[i].view(-1).view(torch_uint8()), non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def d2h_bytes(self):
+        return _nbytes(self.dst_init) * len(self.w.ops)
+
+    def config(self):
+        w = self.w
+        return {"workload": w.name, "op": "TREDUCE", "nranks": w.nranks, "storage_dtype": self.storage,
+                "shape": [w.rows, w.cols], "ld": w.ld, "valid": [w.valid_rows, w.valid_cols],
+                "ops": w.ops, "root": w.root, "values": "%s%s" % (w.dist[0], list(w.dist[1:])),
+                "seed": "1234 + rank (SplitMix64, counter-based)",
+                "step": "%d TREDUCE launches (%s)" % (len(w.ops), ", ".join(w.ops)),
+                "bytes_per_step": self.bytes_per_step(),
+                "l2": "flushed before every step (256 MiB device write, outside the timed events)"}
+
+    # oracle on a bounded sample: the first `rows` rows of the valid box
+    def oracle_sample(self, rows):
+        import oracle
+        w = self.w
+        rows = max(1, min(rows, w.valid_rows))
+        import numpy as np
+        out = np.empty((rows, w.ld), dtype=self.host[0].dtype)
+        code = {"f32": oracle.F32, "bf16": oracle.BF16, "f16": oracle.F16, "i32": oracle.I32}[self.storage]
+        ops = {"sum": oracle.SUM, "max": oracle.MAX, "min": oracle.MIN}
+        t0 = time.perf_counter()
+        for op in w.ops:
+            oracle.treduce(self.host, out, rows, w.valid_cols, w.ld, ops[op], code)
+        dt = time.perf_counter() - t0
+        nbytes = (w.nranks + 1) * w.elem_bytes * rows * w.valid_cols * len(w.ops)
+        return nbytes, dt, "rows 0..%d of the %dx%d valid box, ops %s" % (
+            rows - 1, w.valid_rows, w.valid_cols, "+".join(w.ops))
+
+    def oracle_rows_per_second(self):
+        nb, dt, _ = self.oracle_sample(8)
+        return 8.0 / max(dt, 1e-9)
+
+
+class RsAgBench(Workload):
+    """reduce_scatter (Sum) then allgather over 8 fp16 windows [8192, 4096]."""
+
+    def __init__(self):
+        import synth
+        self.cfg = synth.CONFIG4
+        self.name = "reduce_scatter_allgather_n8_f16_8192x4096"
+        self.storage = "f16"
+        self.kernel = "reduce_kernel (f16, scatter) + gather_kernel"
+
+    def bytes_per_launch_list(self):
+        c = self.cfg
+        elems = c["rows"] * c["cols"]
+        return [(c["nranks"] + 1) * 2 * elems, c["nranks"] * 2 * elems]
+
+    def launches_per_step(self):
+        return 2
+
+    def bytes_per_step(self):
+        return sum(self.bytes_per_launch_list())
+
+    def bytes_per_launch(self):
+        return self.bytes_per_launch_list()[0]
+
+    def setup_host(self):
+        import synth
+        self.host = [synth.window(r) for r in range(self.cfg["nranks"])]
+
+    def setup_device(self, dev):
+        self.dev = [_to_dev(h, dev) for h in self.host]
+
+    def launch(self, i, srcs=None, dst=None):
+        import tile_level_collective_gb300 as P
+        c = self.cfg
+        wins = srcs or self.dev
+        if i == 0:
+            P.ptoc_reduce_scatter(wins, c["rows"], c["cols"], c["ld"], P.SUM, P.F16)
+        else:
+            P.ptoc_allgather(wins, c["rows"], c["cols"], c["ld"], P.F16)
+
+    def setup_e2e(self, dev):
+        import torch
+        self.pinned = [_pin(h) for h in self.host]
+        self.out_pinned = [torch.empty(_nbytes(h), dtype=torch.uint8).pin_memory() for h in self.host]
+        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+
+    def e2e_step(self):
+        for d, h in zip(self.e2e_dev, self.pinned):
+            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+        self.launch(0, srcs=self.e2e_dev)
+        self.launch(1, srcs=self.e2e_dev)
+        for d, o in zip(self.e2e_dev, self.out_pinned):
+            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def d2h_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def config(self):
+        c = self.cfg
+        return {"workload": self.name, "op": "reduce_scatter+allgather", "nranks": c["nranks"],
+                "storage_dtype": "f16", "shape": [c["rows"], c["cols"]], "ld": c["ld"],
+                "values": "normal(0,1)", "step": "reduce_scatter (Sum) then allgather",
+                "bytes_per_step": self.bytes_per_step(),
+                "l2": "flushed before every step (256 MiB device write, outside the timed events)"}
+
+    def oracle_sample(self, rows):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        n = c["nranks"]
+        rows = max(n, min(rows, c["rows"]))
+        wins = [np.ascontiguousarray(h[:rows]) for h in self.host]
+        t0 = time.perf_counter()
+        oracle.reduce_scatter(wins, rows, c["cols"], c["ld"], oracle.SUM, oracle.F16)
+        oracle.allgather(wins, rows, c["cols"], c["ld"], oracle.F16)
+        dt = time.perf_counter() - t0
+        nb = (2 * n + 1) * 2 * rows * c["cols"]
+        return nb, dt, "reduce_scatter+allgather over rows 0..%d of the 8 windows" % (rows - 1)
+
+    def oracle_rows_per_second(self):
+        nb, dt, _ = self.oracle_sample(64)
+        return 64.0 / max(dt, 1e-9)
+
+
+class A2avBench(Workload):
+    """all_to_all_v: 16 ranks, bf16 rows of 7168, target_rows 24576."""
+
+    def __init__(self):
+        import synth
+        self.cfg = synth.CONFIG5
+        self.name = "all_to_all_v_n16_bf16_7168_maxrecv1536"
+        self.storage = "bf16"
+        self.kernel = "a2av_kernel"
+        self.dtype_compute = "u16"
+
+    def setup_host(self):
+        import numpy as np
+        import synth
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        self.mr = tr // n
+        self.host = [synth.a2av_input(s, n, tr, size) for s in range(n)]
+        self.sc = [synth.a2av_send_counts(s, n) for s in range(n)]
+        moved = sum(int(np.clip(c_, 0, self.mr).sum()) for c_ in self.sc)
+        self.moved_rows = moved
+
+    def bytes_per_launch(self):
+        n = self.cfg["nranks"]
+        return 2 * 2 * self.cfg["size"] * self.moved_rows + 8 * n * n
+
+    def launches_per_step(self):
+        return 1
+
+    def bytes_per_step(self):
+        return self.bytes_per_launch()
+
+    def setup_device(self, dev):
+        import torch
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        self.dev = [_to_dev(h, dev) for h in self.host]
+        self.d_sc = [_to_dev(x, dev) for x in self.sc]
+        self.d_tg = [torch.full((tr, size), -1, dtype=torch.int16, device=dev) for _ in range(n)]
+        self.d_rc = [torch.zeros(n, dtype=torch.int32, device=dev) for _ in range(n)]
+
+    def launch(self, i, srcs=None, dst=None):
+        import tile_level_collective_gb300 as P
+        c = self.cfg
+        P.ptoc_all_to_all_v(srcs or self.dev, self.d_tg, self.d_sc, self.d_rc, c["target_rows"], c["size"],
+                            P.BF16)
+
+    def setup_e2e(self, dev):
+        import torch
+        self.pinned = [_pin(h) for h in self.host]
+        self.out_pinned = [torch.empty(_nbytes(h), dtype=torch.uint8).pin_memory() for h in self.host]
+        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+
+    def e2e_step(self):
+        for d, h in zip(self.e2e_dev, self.pinned):
+            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+        self.launch(0, srcs=self.e2e_dev)
+        for d, o in zip(self.d_tg, self.out_pinned):
+            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def d2h_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def config(self):
+        c = self.cfg
+        return {"workload": self.name, "op": "all_to_all_v", "nranks": c["nranks"], "storage_dtype": "bf16",
+                "row_elems": c["size"], "target_rows": c["target_rows"], "max_recv": self.mr,
+                "send_counts": "uniform int [0, 2047] per (src, dest), seed 1234 + src",
+                "moved_rows": self.moved_rows, "bytes_per_step": self.bytes_per_step(),
+                "l2": "flushed before every step (256 MiB device write, outside the timed events)"}
+
+    def oracle_sample(self, rows):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        n, size = c["nranks"], c["size"]
+        # the same exchange with every count scaled into [0, rows]: a bounded sample
+        mr = max(1, min(rows, self.mr))
+        tr = mr * n
+        ins = [np.ascontiguousarray(h.reshape(n, self.mr, size)[:, :mr].reshape(tr, size)) for h in self.host]
+        tg = [np.empty((tr, size), dtype=np.uint16) for _ in range(n)]
+        sc = [np.ascontiguousarray(np.clip(x, 0, self.mr) * mr // self.mr).astype(np.int32) for x in self.sc]
+        rc = [np.zeros(n, dtype=np.int32) for _ in range(n)]
+        t0 = time.perf_counter()
+        oracle.all_to_all_v(ins, tg, sc, rc, tr, size, 2)
+        dt = time.perf_counter() - t0
+        moved = sum(int(x.sum()) for x in rc)
+        return 4 * size * moved, dt, "the exchange with capacity %d rows per pair (counts scaled)" % mr
+
+    def oracle_rows_per_second(self):
+        nb, dt, _ = self.oracle_sample(16)
+        return 16.0 / max(dt, 1e-9)
+
+
+def make_workload(name):
+    import synth
+    if name in ("treduce", "treduce_bf16"):
+        return TreduceBench(synth.config2(), "bf16")
+    if name == "treduce_small":
+        return TreduceBench(synth.config1(), "f32")
+    if name == "treduce_f32":
+        return TreduceBench(synth.config3(), "f32")
+    if name == "treduce_i32":
+        return TreduceBench(synth.config3_int(), "i32")
+    if name == "rs_ag":
+        return RsAgBench()
+    if name == "a2av":
+        return A2avBench()
+    raise SystemExit("unknown workload %s" % name)
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def torch_uint8():
+    import torch
+    return torch.uint8
+
+
+def _nbytes(a):
+    return int(a.nbytes) if hasattr(a, "nbytes") else a.numel() * a.element_size()
+
+
+def _to_dev(h, dev):
+    import numpy as np
+    import torch
+    h = np.ascontiguousarray(h)
+    t = torch.from_numpy(h.view(np.int16) if h.dtype == np.uint16 else h)
+    return t.to(dev)
+
+
+def _pin(h):
+    import numpy as np
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(h).reshape(-1).view(np.uint8)).pin_memory()
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (copy, burst): of measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s: of fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per launch recorded from an ncu capture of the current
+    kernel sources (profiles/traffic.txt lines: workload sha bytes), else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload_name and parts[1] == sha:
+            return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        inside = [r for t, r in self.rows if t0 <= t <= t1]
+        note = []
+        if not inside:
+            inside = [min(self.rows, key=lambda x: abs(x[0] - (t0 + t1) / 2))[1]]
+            note = ["nearest sample (timed region shorter than the sampling period)"]
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons) + note, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle as it stands, single-threaded, on a sample of the workload
+    (at most the whole step), repeated to about `budget_s` seconds of CPU
+    work."""
+    rps = wl.oracle_rows_per_second()
+    rows = max(1, int(rps * budget_s))
+    nb_tot, dt_tot, reps, desc = 0, 0.0, 0, ""
+    while dt_tot < budget_s or reps == 0:
+        nb, dt, desc = wl.oracle_sample(rows)
+        nb_tot, dt_tot, reps = nb_tot + nb, dt_tot + dt, reps + 1
+    return {"value": nb_tot / dt_tot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%s, %d repetition(s)" % (desc, reps), "seconds": round(dt_tot, 3)}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    wl = make_workload(args.workload)
+    wl.setup_host()
+    wl.setup_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nl = wl.launches_per_step()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        for i in range(nl):
+            wl.launch(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    if sampler:
+        time.sleep(0.6)          # let the sampler start before the timed region
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+          for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        for i in range(nl):
+            ev[k][i][0].record(stream)
+            wl.launch(i)
+            ev[k][i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    if sampler:
+        sampler.stop()
+    per_launch = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(nl)] for k in range(args.steps)]
+    # a step = its launches back to back on the stream (the flush between steps excluded)
+    step_ms = [sum(x) for x in per_launch]
+    ms_local = sum(step_ms) / args.steps
+    ms = max_over_ranks(ms_local, world, dev)
+    value = world * wl.bytes_per_step() / (ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel: launch 0's family
+    avg0 = statistics.mean(x[0] for x in per_launch) if nl == 1 or args.workload == "rs_ag" else \
+        statistics.mean(v for x in per_launch for v in x)
+    achieved = wl.bytes_per_launch() / (avg0 / 1e3) / 1e9
+    peak, peak_src = measured_peak()
+    traffic = recorded_traffic(wl.name)
+
+    # end to end: pinned host inputs in, results out, every step
+    wl.setup_e2e(dev)
+    for _ in range(max(1, min(args.warmup, 3))):
+        wl.e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.e2e_steps, args.steps))
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    es.record(stream)
+    for _ in range(e_steps):
+        wl.e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(es.elapsed_time(ee) / e_steps, world, dev)
+    e_value = world * wl.bytes_per_step() / (e_ms / 1e3) / 1e9
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype_compute, "data": "synthetic (seeded SplitMix64, generated on the host)",
+        "config": dict(wl.config(), parallelism="replicas" if world > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": wl.kernel,
+                     "bytes_per_launch": wl.bytes_per_launch(), "avg_launch_ms": round(avg0, 6),
+                     "peak_source": peak_src},
+        "e2e": {"value": round(e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes(),
+                "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": round(e_ms, 6),
+                "path": "pinned host -> device copy, the library calls, device -> pinned host copy"},
+        "gpu_launches": nl * args.steps,
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The oracle on the host cores, each step a bounded sample of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = make_workload(args.workload)
+    wl.setup_host()
+    total_steps = args.steps + args.warmup
+    per_step = max(0.002, args.reference_seconds / max(1, total_steps))
+    rows = max(1, int(wl.oracle_rows_per_second() * per_step))
+    for _ in range(args.warmup):
+        wl.oracle_sample(rows)
+    nb_tot, dt_tot, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        nb, dt, desc = wl.oracle_sample(rows)
+        nb_tot += nb
+        dt_tot += dt
+    value = nb_tot / dt_tot / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt_tot / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype_compute, "data": "synthetic",
+        "config": wl.config(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="treduce",
+                    choices=["treduce", "treduce_bf16", "treduce_small", "treduce_f32", "treduce_i32",
+                             "rs_ag", "a2av"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * ptoc.h - C ABI of the GB300 tile-level collective library (libptoc.so).
+ *
+ * The library computes the data-parallel core of the PTO communication ops on
+ * N symmetric per-rank window buffers that all live in ONE GPU's memory: the
+ * TREDUCE element-wise reduction and the window-layout data movement of
+ * reduce_scatter, allgather and all_to_all_v. Sources, cited by page title and
+ * section:
+ *   [TR] "CANN PTO-ISA TREDUCE 指令详解" (TREDUCE instruction explained,
+ *        lpnh.cn news 2291107), sections 1-8.
+ *   [DO] "Distributed Operators (N6)" (pypto.ai dev/distributed_ops): the op
+ *        table in "Overview", "ABI enums", "pld.tensor.all_to_all_v",
+ *        "pld.tensor.allreduce".
+ *
+ * Conventions shared by every entry point
+ *   - Every data pointer is a DEVICE pointer on the calling thread's current
+ *     CUDA device. Pointer arrays (ptoc_group.tensors, send_counts,
+ *     recv_counts) are HOST arrays of device pointers; they are read during
+ *     the call and copied into kernel parameters, so the caller may free or
+ *     reuse them as soon as the call returns.
+ *   - The caller owns every buffer. The library allocates no device or host
+ *     memory and keeps no per-call state.
+ *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
+ *     stream). Completion is observed through the stream; results must not be
+ *     read, and inputs must not be modified, before the stream reaches them.
+ *   - Layout: a "slice" is row-major with a row pitch of `ld` ELEMENTS
+ *     (ld >= cols). Element (i, j) is at offset i*ld + j. The footprint the
+ *     library may touch is (rows-1)*ld + cols elements from the base pointer.
+ *   - Every pointer must be aligned to its element size. Wider alignment
+ *     (16 bytes for base pointers and ld*elem_size) selects faster kernels.
+ *   - Errors are returned synchronously and NOTHING is launched when a call
+ *     returns anything but PTOC_OK. A CUDA launch failure is PTOC_ERR_CUDA.
+ *   - Floating point: accumulation in binary32 for f32, f16 and bf16 with one
+ *     round-to-nearest-even narrowing per output element; subnormals kept;
+ *     Sum adds one rank at a time in the documented rank order (no fused or
+ *     reassociated arithmetic). int32 Sum wraps modulo 2^32.
+ */
+#ifndef PTOC_H
+#define PTOC_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest group the library accepts (kernel parameters hold one pointer per
+ * rank). */
+#define PTOC_MAX_RANKS 64
+
+typedef enum {
+    PTOC_OK = 0,
+    PTOC_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum, misalignment */
+    PTOC_ERR_UNSUPPORTED = 2,   /* a valid enum value this library does not implement */
+    PTOC_ERR_ALIAS = 3,         /* an output overlaps another operand */
+    PTOC_ERR_CUDA = 4           /* the CUDA runtime reported an error at launch */
+} ptoc_status;
+
+/* Reduction operators. Values follow the ReduceOp ABI ([TR] §1.3: Sum = 0,
+ * Max = 1, Min = 2; [DO] "ABI enums" appends kProd = 3, which this library
+ * reserves: PTOC_PROD returns PTOC_ERR_UNSUPPORTED). */
+typedef enum {
+    PTOC_SUM = 0,
+    PTOC_MAX = 1,
+    PTOC_MIN = 2,
+    PTOC_PROD = 3
+} ptoc_reduce_op;
+
+/* Element types. f16 / bf16 are IEEE binary16 and bfloat16 encodings. */
+typedef enum {
+    PTOC_F32 = 0,
+    PTOC_F16 = 1,
+    PTOC_BF16 = 2,
+    PTOC_I32 = 3
+} ptoc_dtype;
+
+/* A rank group ([TR] §2.1, §3.3, §6: ParallelGroup{tensors, nranks, rootIdx}).
+ * tensors: host array of nranks device pointers, tensors[r] = rank r's slice.
+ * Requires 1 <= nranks <= PTOC_MAX_RANKS; root in [0, nranks) where used. All
+ * slices share one shape and row pitch. */
+typedef struct {
+    void* const* tensors;
+    int32_t nranks;
+    int32_t root;
+} ptoc_group;
+
+/*
+ * ptoc_treduce - TREDUCE ([TR] §1.1, §4).
+ *   dst[i*ld + j] = (+)_{r} tensors[r][i*ld + j]
+ * for i < valid_rows, j < valid_cols, with (+) = op. rows x cols is the
+ * physical box of every slice and of dst (valid_rows <= rows,
+ * valid_cols <= cols <= ld). Only the valid box is read, and only the valid
+ * box of dst is written: padding is never touched ([TR] §3.4, §4.2).
+ *
+ * Order: the root's element starts the accumulation, then every other rank in
+ * ascending order, skipping the root ([TR] §4.3). Max / Min keep the earlier
+ * operand on ties (+0 / -0 included) and never let a NaN replace the
+ * accumulator; their result is the selected input element, bit for bit.
+ * nranks == 1 is a bit copy ([TR] §4.3). An empty valid box returns PTOC_OK
+ * and launches nothing ([TR] §4.1).
+ *
+ * dst may be exactly tensors[root] (in place); any other overlap between dst's
+ * valid footprint and a source's is PTOC_ERR_ALIAS. Sources may alias each
+ * other.
+ */
+ptoc_status ptoc_treduce(const ptoc_group* group, void* dst,
+                         int64_t rows, int64_t cols,
+                         int64_t valid_rows, int64_t valid_cols, int64_t ld,
+                         ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream);
+
+/*
+ * ptoc_reduce_scatter - reduce_scatter over N windows, in place ([DO] op
+ * table: "reduce and scatter chunks across ranks"; the result is the window).
+ * Window r's row chunk [floor(r*rows/N), floor((r+1)*rows/N)) (the balanced
+ * segment bounds of [DO] "pld.tensor.allreduce", ring mode, applied to rows)
+ * becomes the reduction over all windows of the same rows, columns
+ * [0, cols), in rank order 0..N-1, binary32 accumulation. Every other element
+ * of every window is left unchanged. windows->root is ignored.
+ * Windows must not overlap one another (PTOC_ERR_ALIAS).
+ */
+ptoc_status ptoc_reduce_scatter(const ptoc_group* windows,
+                                int64_t rows, int64_t cols, int64_t ld,
+                                ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream);
+
+/*
+ * ptoc_allgather - allgather over N windows, in place ([DO] op table: "gather
+ * data from all ranks via window"). Row chunk r (bounds as in
+ * ptoc_reduce_scatter) of window r is copied bit for bit into row chunk r of
+ * every other window, columns [0, cols). Called after ptoc_reduce_scatter
+ * with the same arguments it leaves every window equal to the full reduction.
+ * windows->root is ignored. Windows must not overlap (PTOC_ERR_ALIAS).
+ */
+ptoc_status ptoc_allgather(const ptoc_group* windows,
+                           int64_t rows, int64_t cols, int64_t ld,
+                           ptoc_dtype dtype, cudaStream_t stream);
+
+/*
+ * ptoc_all_to_all_v - variable-size all-to-all into flat staging windows
+ * ([DO] "pld.tensor.all_to_all_v").
+ *   inputs->tensors[s]  : rank s's packed input  [target_rows, size] (read)
+ *   targets->tensors[d] : rank d's packed window [target_rows, size] (written)
+ *   send_counts[s]      : host array of N device pointers, each int32[N]:
+ *                         rows rank s sends to each destination (read)
+ *   recv_counts[d]      : host array of N device pointers, each int32[N]
+ *                         (the [NR, 1] column): written with the counts rank d
+ *                         receives from each source.
+ * With MAX_RECV = target_rows / N (floor), for every pair (s, d), s == d
+ * included:
+ *   c = clamp(send_counts[s][d], 0, MAX_RECV)            (two-sided clamp)
+ *   recv_counts[d][s] = c
+ *   targets[d] rows [s*MAX_RECV, s*MAX_RECV + c) = inputs[s] rows
+ *                   [d*MAX_RECV, d*MAX_RECV + c)
+ * Target rows outside the counts are never written. Counts live on the
+ * device and are clamped there: out-of-range counts are not errors. The data
+ * is moved bit for bit; dtype only fixes the element size.
+ * inputs->nranks must equal targets->nranks; roots are ignored. Outputs
+ * (targets, recv_counts) must not overlap each other or any input
+ * (PTOC_ERR_ALIAS); inputs and send_counts may overlap one another.
+ */
+ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* targets,
+                              const int32_t* const* send_counts, int32_t* const* recv_counts,
+                              int64_t target_rows, int64_t size, ptoc_dtype dtype,
+                              cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* ptoc_status_string(ptoc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTOC_H */

@@ -1,0 +1,128 @@
+"""The C ABI without a GPU: the library loads, exports every function
+include/ptoc.h declares, and rejects bad arguments with the documented status
+before any CUDA call. Every case here breaks at least one rule (or is empty),
+so no case can reach a kernel launch, on this machine or on a GPU machine.
+Device addresses below are fake and never dereferenced."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tile_level_collective_gb300 as P
+from conftest import ROOT
+
+A = 0x7F0000000000          # fake, 4 KiB-aligned device addresses
+MB = 1 << 20
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ptoc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ptoc_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == ["ptoc_all_to_all_v", "ptoc_allgather", "ptoc_reduce_scatter",
+                                    "ptoc_status_string", "ptoc_treduce"]
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(P.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert P.ptoc_status_string(P.OK) == "PTOC_OK"
+    assert P.ptoc_status_string(P.ERR_ALIAS) == "PTOC_ERR_ALIAS"
+    assert P.ptoc_status_string(P.ERR_UNSUPPORTED) == "PTOC_ERR_UNSUPPORTED"
+    assert P.ptoc_status_string(99) == "PTOC_ERR_UNKNOWN"
+
+
+def srcs(n, stride=64 * MB, base=A):
+    return [base + r * stride for r in range(n)]
+
+
+DST = A + 200 * 64 * MB
+
+
+def tr(tensors=None, dst=DST, rows=8, cols=8, vr=8, vc=8, ld=8, op=P.SUM, dt=P.F32, root=0):
+    tensors = srcs(4) if tensors is None else tensors
+    return P.ptoc_treduce(tensors, dst, rows, cols, vr, vc, ld, op, dt, stream=0, root=root, check=False)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(tensors=[]), P.ERR_INVALID_ARG),                       # nranks 0
+    (dict(tensors=srcs(65, stride=MB)), P.ERR_INVALID_ARG),      # nranks > 64
+    (dict(root=-1), P.ERR_INVALID_ARG),                          # root outside [0, N)
+    (dict(root=4), P.ERR_INVALID_ARG),
+    (dict(tensors=[A, 0, A + 2 * 64 * MB, A + 3 * 64 * MB]), P.ERR_INVALID_ARG),  # null slice
+    (dict(dst=0), P.ERR_INVALID_ARG),
+    (dict(dt=7), P.ERR_INVALID_ARG),
+    (dict(op=P.PROD), P.ERR_UNSUPPORTED),                        # reserved ABI value
+    (dict(op=9), P.ERR_INVALID_ARG),
+    (dict(rows=-1), P.ERR_INVALID_ARG),
+    (dict(vr=9), P.ERR_INVALID_ARG),                             # valid > physical
+    (dict(vc=9), P.ERR_INVALID_ARG),
+    (dict(cols=9, vc=8, ld=8), P.ERR_INVALID_ARG),               # cols > ld
+    (dict(ld=-3), P.ERR_INVALID_ARG),
+    (dict(dst=DST + 2), P.ERR_INVALID_ARG),                      # f32 dst not 4-byte aligned
+    (dict(tensors=[A + 1, A + 64 * MB]), P.ERR_INVALID_ARG),     # misaligned source
+    (dict(rows=2 ** 40, cols=2 ** 40, vr=1, vc=1, ld=2 ** 40), P.ERR_INVALID_ARG),  # size overflow
+    (dict(dst=A + 64 * MB + 16), P.ERR_ALIAS),                   # dst overlaps rank 1
+    (dict(dst=A + 64 * MB, root=0), P.ERR_ALIAS),                # dst == a non-root slice
+])
+def test_treduce_rejects(kw, status):
+    assert tr(**kw) == status
+
+
+def test_treduce_empty_region_is_ok_without_launch():
+    assert tr(vr=0) == P.OK
+    assert tr(vc=0) == P.OK
+    assert tr(rows=0, cols=0, vr=0, vc=0, ld=0) == P.OK
+
+
+def test_treduce_raises_ptoc_error():
+    with pytest.raises(P.PtocError) as e:
+        P.ptoc_treduce(srcs(2), DST, 4, 4, 4, 4, 4, P.PROD, P.F32, stream=0)
+    assert e.value.status == P.ERR_UNSUPPORTED
+
+
+def test_reduce_scatter_and_allgather_reject():
+    w = srcs(4)
+    overl = [A, A + 100, A + 2 * 64 * MB, A + 3 * 64 * MB]
+    assert P.ptoc_reduce_scatter(overl, 64, 64, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_ALIAS
+    assert P.ptoc_reduce_scatter(w, 64, 64, 64, P.PROD, P.F32, stream=0, check=False) == P.ERR_UNSUPPORTED
+    assert P.ptoc_reduce_scatter(w, 64, 65, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_reduce_scatter(w, 64, 64, 64, P.SUM, 5, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_reduce_scatter([], 64, 64, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_reduce_scatter(w, 0, 64, 64, P.SUM, P.F32, stream=0, check=False) == P.OK
+    assert P.ptoc_allgather(overl, 64, 64, 64, P.F16, stream=0, check=False) == P.ERR_ALIAS
+    assert P.ptoc_allgather([A + 1, A + 64 * MB], 4, 4, 4, P.F16, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_allgather(w, 64, 0, 64, P.F16, stream=0, check=False) == P.OK
+    assert P.ptoc_allgather([A], 64, 64, 64, P.F16, stream=0, check=False) == P.OK   # one rank: nothing to move
+
+
+def a2av(inputs=None, targets=None, sc=None, rc=None, tr_=64, size=16, dt=P.BF16):
+    n = 4
+    inputs = srcs(n) if inputs is None else inputs
+    targets = srcs(n, base=A + 8 * 64 * MB) if targets is None else targets
+    sc = [A + 16 * 64 * MB + 256 * r for r in range(n)] if sc is None else sc
+    rc = [A + 17 * 64 * MB + 256 * r for r in range(n)] if rc is None else rc
+    return P.ptoc_all_to_all_v(inputs, targets, sc, rc, tr_, size, dt, stream=0, check=False)
+
+
+def test_all_to_all_v_rejects():
+    assert a2av(targets=srcs(3, base=A + 8 * 64 * MB)) == P.ERR_INVALID_ARG        # N mismatch
+    assert a2av(sc=[A + 16 * 64 * MB, 0, A + 16 * 64 * MB + 512, A + 16 * 64 * MB + 768]) == P.ERR_INVALID_ARG
+    assert a2av(rc=[A + 17 * 64 * MB + 2, A + 17 * 64 * MB + 256, A + 17 * 64 * MB + 512,
+                    A + 17 * 64 * MB + 768]) == P.ERR_INVALID_ARG                  # counts misaligned
+    assert a2av(tr_=-1) == P.ERR_INVALID_ARG
+    assert a2av(size=-1) == P.ERR_INVALID_ARG
+    assert a2av(dt=11) == P.ERR_INVALID_ARG
+    # outputs overlapping anything
+    assert a2av(targets=[A] + srcs(3, base=A + 9 * 64 * MB)) == P.ERR_ALIAS                 # target = input
+    assert a2av(targets=[A + 8 * 64 * MB, A + 8 * 64 * MB + 64] + srcs(2, base=A + 10 * 64 * MB)) == P.ERR_ALIAS
+    assert a2av(rc=[A + 16 * 64 * MB + 4] + [A + 17 * 64 * MB + 256 * r for r in range(1, 4)]) == P.ERR_ALIAS
+    assert a2av(rc=[A + 8 * 64 * MB + 8] + [A + 17 * 64 * MB + 256 * r for r in range(1, 4)]) == P.ERR_ALIAS

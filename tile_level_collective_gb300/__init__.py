@@ -1,0 +1,184 @@
+"""GB300 tile-level collective library: Python binding of libptoc.so.
+
+This module only marshals arguments into the C ABI declared in
+``include/ptoc.h``; every step of every operation runs in the library's CUDA
+kernels. PyTorch is used for device memory and streams (``data_ptr()`` and
+``cuda_stream``), never for the computation.
+
+Entry points carry the C names:
+
+    ptoc_treduce(tensors, dst, rows, cols, valid_rows, valid_cols, ld, op, dtype,
+                 stream=None, root=0)
+    ptoc_reduce_scatter(windows, rows, cols, ld, op, dtype, stream=None)
+    ptoc_allgather(windows, rows, cols, ld, dtype, stream=None)
+    ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows,
+                      size, dtype, stream=None)
+
+Buffers are torch tensors or raw device addresses (ints). ``stream=None``
+means torch's current stream. A non-OK status raises :class:`PtocError`
+(nothing was launched); pass ``check=False`` to get the status instead.
+``treduce`` / ``reduce_scatter`` / ``allgather`` / ``all_to_all_v`` are
+shape-inferring conveniences over the same calls.
+
+The package refuses to import when libptoc.so has not been built: there is no
+fallback path.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libptoc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libptoc.so is not built (expected at %s); build it with "
+        "`python -m tile_level_collective_gb300._build` or __graft_entry__.build()" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- ABI constants (mirror include/ptoc.h) ---------------------------------
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA = 0, 1, 2, 3, 4
+SUM, MAX, MIN, PROD = 0, 1, 2, 3
+F32, F16, BF16, I32 = 0, 1, 2, 3
+MAX_RANKS = 64
+
+OPS = {"sum": SUM, "max": MAX, "min": MIN, "prod": PROD}
+
+
+class ptoc_group(ctypes.Structure):
+    _fields_ = [("tensors", ctypes.POINTER(ctypes.c_void_p)),
+                ("nranks", ctypes.c_int32),
+                ("root", ctypes.c_int32)]
+
+
+_vp, _i64 = ctypes.c_void_p, ctypes.c_int64
+_G = ctypes.POINTER(ptoc_group)
+_lib.ptoc_treduce.argtypes = [_G, _vp, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]
+_lib.ptoc_reduce_scatter.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]
+_lib.ptoc_allgather.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, _vp]
+_lib.ptoc_all_to_all_v.argtypes = [_G, _G, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i64, _i64,
+                                   ctypes.c_int, _vp]
+for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v"):
+    getattr(_lib, _f).restype = ctypes.c_int
+_lib.ptoc_status_string.argtypes = [ctypes.c_int]
+_lib.ptoc_status_string.restype = ctypes.c_char_p
+
+
+class PtocError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s failed: %s" % (where, ptoc_status_string(status)))
+
+
+def ptoc_status_string(status):
+    return _lib.ptoc_status_string(int(status)).decode()
+
+
+def _addr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        if torch.cuda.is_available() and torch.cuda.is_initialized():
+            return torch.cuda.current_stream().cuda_stream
+        return 0
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr_array(items):
+    return (ctypes.c_void_p * max(len(items), 1))(*[_addr(t) for t in items])
+
+
+def _group(tensors, root=0):
+    arr = _ptr_array(tensors)
+    g = ptoc_group(ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)), len(tensors), root)
+    return g, arr
+
+
+def _done(status, where, check):
+    if check and status != OK:
+        raise PtocError(status, where)
+    return status
+
+
+def ptoc_treduce(tensors, dst, rows, cols, valid_rows, valid_cols, ld, op, dtype,
+                 stream=None, root=0, check=True):
+    g, keep = _group(tensors, root)
+    st = _lib.ptoc_treduce(ctypes.byref(g), _addr(dst), rows, cols, valid_rows, valid_cols, ld,
+                           int(op), int(dtype), _stream(stream))
+    return _done(st, "ptoc_treduce", check)
+
+
+def ptoc_reduce_scatter(windows, rows, cols, ld, op, dtype, stream=None, check=True):
+    g, keep = _group(windows)
+    st = _lib.ptoc_reduce_scatter(ctypes.byref(g), rows, cols, ld, int(op), int(dtype), _stream(stream))
+    return _done(st, "ptoc_reduce_scatter", check)
+
+
+def ptoc_allgather(windows, rows, cols, ld, dtype, stream=None, check=True):
+    g, keep = _group(windows)
+    st = _lib.ptoc_allgather(ctypes.byref(g), rows, cols, ld, int(dtype), _stream(stream))
+    return _done(st, "ptoc_allgather", check)
+
+
+def ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows, size, dtype,
+                      stream=None, check=True):
+    gi, k1 = _group(inputs)
+    gt, k2 = _group(targets)
+    sc = _ptr_array(send_counts)
+    rc = _ptr_array(recv_counts)
+    st = _lib.ptoc_all_to_all_v(ctypes.byref(gi), ctypes.byref(gt), sc, rc, target_rows, size,
+                                int(dtype), _stream(stream))
+    return _done(st, "ptoc_all_to_all_v", check)
+
+
+# ---- shape-inferring conveniences over torch tensors ------------------------
+
+def dtype_code(t):
+    import torch
+    m = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16, torch.int32: I32}
+    if t.dtype not in m:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    return m[t.dtype]
+
+
+def _rows_cols_ld(t):
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.stride(1) != 1:
+        raise ValueError("rows must be contiguous (stride(1) == 1)")
+    return t.shape[0], t.shape[1], t.stride(0)
+
+
+def treduce(tensors, dst, op="sum", valid_rows=None, valid_cols=None, root=0, stream=None):
+    """dst = reduction of 2-D tensors over their valid box (default: all)."""
+    rows, cols, ld = _rows_cols_ld(dst)
+    vr = rows if valid_rows is None else valid_rows
+    vc = cols if valid_cols is None else valid_cols
+    return ptoc_treduce(tensors, dst, rows, cols, vr, vc, ld, OPS[op] if isinstance(op, str) else op,
+                        dtype_code(dst), stream=stream, root=root)
+
+
+def reduce_scatter(windows, op="sum", stream=None):
+    rows, cols, ld = _rows_cols_ld(windows[0])
+    return ptoc_reduce_scatter(windows, rows, cols, ld, OPS[op] if isinstance(op, str) else op,
+                               dtype_code(windows[0]), stream=stream)
+
+
+def allgather(windows, stream=None):
+    rows, cols, ld = _rows_cols_ld(windows[0])
+    return ptoc_allgather(windows, rows, cols, ld, dtype_code(windows[0]), stream=stream)
+
+
+def all_to_all_v(inputs, targets, send_counts, recv_counts, stream=None):
+    tr, size = targets[0].shape
+    return ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, tr, size,
+                             dtype_code(targets[0]), stream=stream)

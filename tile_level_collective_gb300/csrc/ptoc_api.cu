@@ -1,0 +1,374 @@
+// C-ABI entry points of libptoc.so: argument validation, operand ordering,
+// vector-width and grid selection, and the launch. Every check runs on the
+// host before any CUDA call, so a rejected call launches nothing and needs no
+// GPU. Semantics and citations are in include/ptoc.h.
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "ptoc.h"
+#include "ptoc_internal.h"
+
+namespace ptoc {
+namespace {
+
+int elem_size(int dtype)
+{
+    switch (dtype) {
+    case PTOC_F32: case PTOC_I32: return 4;
+    case PTOC_F16: case PTOC_BF16: return 2;
+    default: return 0;
+    }
+}
+
+bool valid_dtype(int dtype) { return elem_size(dtype) != 0; }
+
+// op: Sum / Max / Min are implemented; Prod is a reserved ABI value.
+ptoc_status check_op(int op)
+{
+    if (op == PTOC_SUM || op == PTOC_MAX || op == PTOC_MIN) return PTOC_OK;
+    if (op == PTOC_PROD) return PTOC_ERR_UNSUPPORTED;
+    return PTOC_ERR_INVALID_ARG;
+}
+
+// Byte range [lo, hi) a buffer occupies.
+struct Range {
+    uintptr_t lo, hi;
+};
+
+bool overlap(const Range& a, const Range& b) { return a.lo < b.hi && b.lo < a.hi && a.lo < a.hi && b.lo < b.hi; }
+
+// Footprint in bytes of a [rows, cols] box with pitch ld, or -1 on overflow.
+int64_t footprint(int64_t rows, int64_t cols, int64_t ld, int eb)
+{
+    if (rows == 0 || cols == 0) return 0;
+    const int64_t lim = INT64_MAX / 8;
+    if (rows > lim / (ld > 0 ? ld : 1)) return -1;
+    const int64_t elems = (rows - 1) * ld + cols;
+    if (elems > lim / eb) return -1;
+    return elems * eb;
+}
+
+// The widest vector (16, 8, 4 or 2 bytes) that every address and the pitch
+// allow, never narrower than one element (addresses are element-aligned).
+int pick_vector_bytes(uintptr_t addr_or, int64_t pitch_bytes, int eb)
+{
+    const uintptr_t m = addr_or | (uintptr_t)pitch_bytes;
+    for (int vb = 16; vb > eb; vb >>= 1)
+        if ((m & (uintptr_t)(vb - 1)) == 0) return vb;
+    return eb;
+}
+
+std::atomic<int> g_sm_count[64];
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev < 64) {
+        int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int c = 1;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 1;
+    if (dev < 64) g_sm_count[dev].store(c, std::memory_order_relaxed);
+    return c;
+}
+
+// Optional A/B switch for measurements: PTOC_UNROLL=1|2 (vectors per thread
+// per tile in the reductions). Default 1: 2 doubles the registers of the
+// 16-byte kernels (one resident CTA per SM instead of two) for the same bytes
+// in flight per SM.
+int reduce_unroll(int vb)
+{
+    const char* e = getenv("PTOC_UNROLL");
+    if (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) return e[0] - '0';
+    return 1;
+}
+
+// Tile description of a [rows, cols] box with pitch ld for vectors of vb
+// bytes and tiles of `tile_vec` vectors.
+struct Box {
+    int64_t rows, ld, vpr, tpr, ntiles;
+    int32_t tail;
+};
+
+Box make_box(int64_t rows, int64_t cols, int64_t ld, int eb, int vb, int tile_vec)
+{
+    Box b;
+    b.rows = rows;
+    b.ld = ld;
+    const int ve = vb / eb;
+    b.vpr = cols / ve;
+    b.tail = (int32_t)(cols - b.vpr * ve);
+    b.tpr = (b.vpr + tile_vec - 1) / tile_vec;
+    if (b.tpr == 0) b.tpr = 1;
+    b.ntiles = rows * b.tpr;
+    return b;
+}
+
+dim3 grid_for(int64_t ntiles)
+{
+    // One tile per CTA; the hardware block scheduler balances the tail. Very
+    // large boxes fall back to a grid-stride loop inside the kernel.
+    const int64_t cap = (int64_t)1 << 30;
+    return dim3((unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap));
+}
+
+cudaError_t launch_reduce(int dtype, const ReduceParams& p, int op, int vb, int unroll, dim3 grid,
+                          cudaStream_t s)
+{
+    switch (dtype) {
+    case PTOC_F32: return launch_reduce_f32(p, op, vb, unroll, grid, s);
+    case PTOC_I32: return launch_reduce_i32(p, op, vb, unroll, grid, s);
+    case PTOC_F16: return launch_reduce_f16(p, op, vb, unroll, grid, s);
+    default: return launch_reduce_bf16(p, op, vb, unroll, grid, s);
+    }
+}
+
+ptoc_status check_group(const ptoc_group* g, bool need_root)
+{
+    if (!g || !g->tensors) return PTOC_ERR_INVALID_ARG;
+    if (g->nranks < 1 || g->nranks > kMaxRanks) return PTOC_ERR_INVALID_ARG;
+    if (need_root && (g->root < 0 || g->root >= g->nranks)) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < g->nranks; ++r)
+        if (!g->tensors[r]) return PTOC_ERR_INVALID_ARG;
+    return PTOC_OK;
+}
+
+bool aligned(const void* p, int eb) { return ((uintptr_t)p % (uintptr_t)eb) == 0; }
+
+// Shared checks of the window collectives (reduce_scatter, allgather).
+ptoc_status check_windows(const ptoc_group* w, int64_t rows, int64_t cols, int64_t ld, int dtype,
+                          int64_t* fp_out)
+{
+    ptoc_status st = check_group(w, false);
+    if (st != PTOC_OK) return st;
+    if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || ld < 0 || (rows > 0 && cols > ld)) return PTOC_ERR_INVALID_ARG;
+    const int eb = elem_size(dtype);
+    const int64_t fp = footprint(rows, cols, ld, eb);
+    if (fp < 0) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < w->nranks; ++r)
+        if (!aligned(w->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
+    for (int a = 0; a < w->nranks; ++a)
+        for (int b = a + 1; b < w->nranks; ++b) {
+            const Range ra{(uintptr_t)w->tensors[a], (uintptr_t)w->tensors[a] + (uintptr_t)fp};
+            const Range rb{(uintptr_t)w->tensors[b], (uintptr_t)w->tensors[b] + (uintptr_t)fp};
+            if (overlap(ra, rb)) return PTOC_ERR_ALIAS;
+        }
+    *fp_out = fp;
+    return PTOC_OK;
+}
+
+}  // namespace
+}  // namespace ptoc
+
+using namespace ptoc;
+
+extern "C" ptoc_status ptoc_treduce(const ptoc_group* group, void* dst, int64_t rows, int64_t cols,
+                                    int64_t valid_rows, int64_t valid_cols, int64_t ld,
+                                    ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
+{
+    ptoc_status st = check_group(group, true);
+    if (st != PTOC_OK) return st;
+    if (!dst) return PTOC_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
+    st = check_op(op);
+    if (st != PTOC_OK) return st;
+    if (rows < 0 || cols < 0 || valid_rows < 0 || valid_cols < 0 || ld < 0) return PTOC_ERR_INVALID_ARG;
+    if (valid_rows > rows || valid_cols > cols || (rows > 0 && cols > ld)) return PTOC_ERR_INVALID_ARG;
+    const int eb = elem_size(dtype);
+    if (footprint(rows, cols, ld, eb) < 0) return PTOC_ERR_INVALID_ARG;
+    const int n = group->nranks;
+    if (!aligned(dst, eb)) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r)
+        if (!aligned(group->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
+
+    // Empty valid region: nothing is read or written (TREDUCE article §4.1).
+    if (valid_rows == 0 || valid_cols == 0) return PTOC_OK;
+
+    // dst may be exactly the root's slice (in place); any other overlap of the
+    // valid footprints is an alias.
+    const int64_t fp = footprint(valid_rows, valid_cols, ld, eb);
+    const Range rd{(uintptr_t)dst, (uintptr_t)dst + (uintptr_t)fp};
+    for (int r = 0; r < n; ++r) {
+        const void* s = group->tensors[r];
+        if (s == dst && r == group->root) continue;
+        const Range rs{(uintptr_t)s, (uintptr_t)s + (uintptr_t)fp};
+        if (overlap(rd, rs)) return PTOC_ERR_ALIAS;
+    }
+
+    ReduceParams p;
+    memset(&p, 0, sizeof(p));
+    // Reduction order (TREDUCE article §4.3): root first, then ascending.
+    int k = 0;
+    p.src[k++] = group->tensors[group->root];
+    for (int r = 0; r < n; ++r)
+        if (r != group->root) p.src[k++] = group->tensors[r];
+    p.dst[0] = dst;
+    p.nranks = n;
+    p.scatter = 0;
+    // One rank: a bit copy (TREDUCE article §4.3). Max with a single operand
+    // is exactly that, NaN payloads included.
+    int eff_op = (n == 1) ? PTOC_MAX : (int)op;
+
+    // Contiguous valid box (full rows, or a single row): one flat row.
+    const bool flat = (valid_cols == ld) || (valid_rows == 1);
+    const int64_t frows = flat ? 1 : valid_rows;
+    const int64_t fcols = flat ? valid_rows * ld - (ld - valid_cols) : valid_cols;
+    const int64_t fld = flat ? fcols : ld;
+    uintptr_t addr_or = (uintptr_t)dst;
+    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)group->tensors[r];
+    const int vb = pick_vector_bytes(addr_or, flat ? 0 : ld * eb, eb);
+    const int unroll = reduce_unroll(vb);
+    const Box b = make_box(frows, fcols, fld, eb, vb, kBlock * unroll);
+    p.ld = b.ld;
+    p.rows = b.rows;
+    p.vpr = b.vpr;
+    p.tail = b.tail;
+    p.tpr = b.tpr;
+    p.ntiles = b.ntiles;
+    cudaError_t e = launch_reduce(dtype, p, eff_op, vb, unroll, grid_for(p.ntiles), stream);
+    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+extern "C" ptoc_status ptoc_reduce_scatter(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                                           ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
+{
+    int64_t fp = 0;
+    ptoc_status st = check_windows(windows, rows, cols, ld, dtype, &fp);
+    if (st != PTOC_OK) return st;
+    st = check_op(op);
+    if (st != PTOC_OK) return st;
+    if (rows == 0 || cols == 0) return PTOC_OK;
+    const int n = windows->nranks;
+    const int eb = elem_size(dtype);
+
+    ReduceParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) {
+        p.src[r] = windows->tensors[r];     // rank order 0..N-1
+        p.dst[r] = windows->tensors[r];     // window r receives its own chunk
+    }
+    p.nranks = n;
+    p.scatter = 1;
+    const int eff_op = (n == 1) ? PTOC_MAX : (int)op;
+    uintptr_t addr_or = 0;
+    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)windows->tensors[r];
+    const int vb = pick_vector_bytes(addr_or, ld * eb, eb);
+    const int unroll = reduce_unroll(vb);
+    const Box b = make_box(rows, cols, ld, eb, vb, kBlock * unroll);
+    p.ld = ld;
+    p.rows = rows;
+    p.vpr = b.vpr;
+    p.tail = b.tail;
+    p.tpr = b.tpr;
+    p.ntiles = b.ntiles;
+    cudaError_t e = launch_reduce(dtype, p, eff_op, vb, unroll, grid_for(p.ntiles), stream);
+    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+extern "C" ptoc_status ptoc_allgather(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                                      ptoc_dtype dtype, cudaStream_t stream)
+{
+    int64_t fp = 0;
+    ptoc_status st = check_windows(windows, rows, cols, ld, dtype, &fp);
+    if (st != PTOC_OK) return st;
+    if (rows == 0 || cols == 0 || windows->nranks == 1) return PTOC_OK;
+    const int n = windows->nranks;
+    const int eb = elem_size(dtype);
+
+    GatherParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) p.win[r] = windows->tensors[r];
+    p.nranks = n;
+    uintptr_t addr_or = 0;
+    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)windows->tensors[r];
+    const int vb = pick_vector_bytes(addr_or, ld * eb, eb);
+    const Box b = make_box(rows, cols, ld, eb, vb, kBlock);
+    p.ld = ld;
+    p.rows = rows;
+    p.vpr = b.vpr;
+    p.tail = b.tail;
+    p.tpr = b.tpr;
+    p.ntiles = b.ntiles;
+    cudaError_t e = launch_gather(p, eb, vb, grid_for(p.ntiles), stream);
+    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* targets,
+                                         const int32_t* const* send_counts, int32_t* const* recv_counts,
+                                         int64_t target_rows, int64_t size, ptoc_dtype dtype,
+                                         cudaStream_t stream)
+{
+    ptoc_status st = check_group(inputs, false);
+    if (st != PTOC_OK) return st;
+    st = check_group(targets, false);
+    if (st != PTOC_OK) return st;
+    if (inputs->nranks != targets->nranks) return PTOC_ERR_INVALID_ARG;
+    if (!send_counts || !recv_counts) return PTOC_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
+    if (target_rows < 0 || size < 0) return PTOC_ERR_INVALID_ARG;
+    const int n = inputs->nranks;
+    const int eb = elem_size(dtype);
+    const int64_t fp = footprint(target_rows, size, size, eb);
+    if (fp < 0) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r) {
+        if (!send_counts[r] || !recv_counts[r]) return PTOC_ERR_INVALID_ARG;
+        if (!aligned(send_counts[r], 4) || !aligned(recv_counts[r], 4)) return PTOC_ERR_INVALID_ARG;
+        if (!aligned(inputs->tensors[r], eb) || !aligned(targets->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
+    }
+
+    // Outputs must not overlap anything (the page requires the five operands
+    // to be pairwise-distinct allocations); inputs may share memory.
+    const uintptr_t cb = (uintptr_t)n * 4u;
+    for (int a = 0; a < n; ++a) {
+        const Range ta{(uintptr_t)targets->tensors[a], (uintptr_t)targets->tensors[a] + (uintptr_t)fp};
+        const Range ra{(uintptr_t)recv_counts[a], (uintptr_t)recv_counts[a] + cb};
+        for (int b = 0; b < n; ++b) {
+            const Range ib{(uintptr_t)inputs->tensors[b], (uintptr_t)inputs->tensors[b] + (uintptr_t)fp};
+            const Range sb{(uintptr_t)send_counts[b], (uintptr_t)send_counts[b] + cb};
+            const Range tb{(uintptr_t)targets->tensors[b], (uintptr_t)targets->tensors[b] + (uintptr_t)fp};
+            const Range rb{(uintptr_t)recv_counts[b], (uintptr_t)recv_counts[b] + cb};
+            if (overlap(ta, ib) || overlap(ta, sb) || overlap(ra, ib) || overlap(ra, sb) || overlap(ta, rb))
+                return PTOC_ERR_ALIAS;
+            if (a != b && (overlap(ta, tb) || overlap(ra, rb))) return PTOC_ERR_ALIAS;
+        }
+    }
+
+    A2avParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) {
+        p.in[r] = inputs->tensors[r];
+        p.tgt[r] = targets->tensors[r];
+        p.sc[r] = send_counts[r];
+        p.rc[r] = recv_counts[r];
+    }
+    p.nranks = n;
+    p.max_recv = target_rows / n;
+    p.row_bytes = size * eb;
+    uintptr_t addr_or = 0;
+    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)inputs->tensors[r] | (uintptr_t)targets->tensors[r];
+    const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
+    p.tile_bytes = (int64_t)vb * kBlock * 4;
+    const int per_sm = a2av_blocks_per_sm(vb, n);
+    dim3 grid((unsigned)(sm_count() * per_sm));
+    cudaError_t e = launch_a2av(p, vb, grid, stream);
+    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+extern "C" const char* ptoc_status_string(ptoc_status s)
+{
+    switch (s) {
+    case PTOC_OK: return "PTOC_OK";
+    case PTOC_ERR_INVALID_ARG: return "PTOC_ERR_INVALID_ARG";
+    case PTOC_ERR_UNSUPPORTED: return "PTOC_ERR_UNSUPPORTED";
+    case PTOC_ERR_ALIAS: return "PTOC_ERR_ALIAS";
+    case PTOC_ERR_CUDA: return "PTOC_ERR_CUDA";
+    default: return "PTOC_ERR_UNKNOWN";
+    }
+}

@@ -1,0 +1,72 @@
+// Internal declarations shared by the library's translation units: kernel
+// parameter blocks (passed by value, so a call needs no device allocation) and
+// the per-dtype launchers the C-ABI layer dispatches to.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+#include "ptoc.h"
+
+namespace ptoc {
+
+constexpr int kMaxRanks = PTOC_MAX_RANKS;
+constexpr int kBlock = 256;          // threads per CTA for every streaming kernel
+
+enum Op : int { kSum = 0, kMax = 1, kMin = 2 };
+
+// TREDUCE and reduce_scatter. The box is `rows` rows of `vpr` full vectors of
+// VB bytes plus `tail` trailing elements; one tile is one row segment of
+// kBlock * U vectors (the last segment of a row also owns the tail).
+struct ReduceParams {
+    const void* src[kMaxRanks];   // sources in reduction order (root first)
+    void* dst[kMaxRanks];         // dst[0] for TREDUCE; window r for reduce_scatter
+    int64_t ld;                   // row pitch, elements
+    int64_t rows;                 // rows of the box (also the scatter chunk basis)
+    int64_t vpr;                  // full vectors per row
+    int64_t tpr;                  // tiles per row
+    int64_t ntiles;               // rows * tpr
+    int32_t tail;                 // elements after the last full vector of a row
+    int32_t nranks;
+    int32_t scatter;              // 1: row i is written to dst[owner(i)]
+};
+
+// allgather: same box description; win[r] is rank r's window.
+struct GatherParams {
+    void* win[kMaxRanks];
+    int64_t ld, rows, vpr, tpr, ntiles;
+    int32_t tail, nranks;
+};
+
+// all_to_all_v: one contiguous segment per (s, d) pair, cut into tiles of
+// tile_bytes; prefix sums over pairs are built in shared memory per CTA.
+struct A2avParams {
+    const void* in[kMaxRanks];
+    void* tgt[kMaxRanks];
+    const int32_t* sc[kMaxRanks];
+    int32_t* rc[kMaxRanks];
+    int64_t max_recv;             // target_rows / nranks
+    int64_t row_bytes;            // size * element bytes
+    int64_t tile_bytes;
+    int32_t nranks;
+};
+
+// Launchers (one translation unit per element type for the reductions).
+// `vb` is the vector width in bytes (16, 8 or 4; 2 for 16-bit data that is
+// only 2-byte aligned). They return the launch status; they never allocate.
+cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
+cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s);
+cudaError_t launch_a2av(const A2avParams& p, int vb, dim3 grid, cudaStream_t s);
+
+// Resident CTAs per SM for each kernel (occupancy query).
+int occupancy_reduce_f32(int op, int vb, int unroll);
+int occupancy_reduce_i32(int op, int vb, int unroll);
+int occupancy_reduce_f16(int op, int vb, int unroll);
+int occupancy_reduce_bf16(int op, int vb, int unroll);
+int a2av_blocks_per_sm(int vb, int nranks);
+size_t a2av_smem_bytes(int nranks);
+
+}  // namespace ptoc

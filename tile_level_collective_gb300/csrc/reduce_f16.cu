@@ -1,0 +1,14 @@
+// TREDUCE / reduce_scatter kernels for __half elements (one translation unit
+// per element type so the library builds in parallel).
+#include "reduce_impl.cuh"
+
+namespace ptoc {
+
+cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s)
+{
+    return launch_reduce_t<__half>(p, op, vb, unroll, grid, s);
+}
+
+int occupancy_reduce_f16(int op, int vb, int unroll) { return occupancy_t<__half>(op, vb, unroll); }
+
+}  // namespace ptoc

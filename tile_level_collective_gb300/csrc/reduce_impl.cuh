@@ -1,0 +1,513 @@
+// TREDUCE / reduce_scatter kernel template.
+//
+// What it computes (TREDUCE article, "CANN PTO-ISA TREDUCE 指令详解", §1.1,
+// §4.3): for every element of the valid box, acc = src[root]; then for every
+// other rank in ascending order acc = acc (+) src[r]; store. The host passes
+// the sources already in that order (src[0] is the root), so the kernel only
+// walks src[0..n-1].
+//
+// How (GB300 design, not the page's UB ping-pong): the op is HBM-bound
+// (N reads + 1 write per element, at most one ALU op per loaded element), so
+// the kernel is a streaming engine. Each thread owns U vectors of VB bytes of
+// one row segment; it issues the loads of a group of up to kGroup ranks
+// back-to-back (U * kGroup independent 16-byte loads in flight per thread) and
+// only then folds them into its accumulator in rank order, so the loads of
+// later ranks overlap the reduction of earlier ones. Accumulation is binary32
+// for every floating type (one RNE narrowing at the store); 16-bit Max / Min
+// compare packed pairs and select the raw encodings, so their result is the
+// selected input bit for bit.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstring>
+#include <type_traits>
+
+#include "ptoc_internal.h"
+
+namespace ptoc {
+
+constexpr int kGroup = 8;   // ranks whose loads are issued together
+
+template <int W>
+struct Words {
+    uint32_t w[W];
+};
+
+template <class To, class From>
+__device__ __forceinline__ To bitcast(const From& f)
+{
+    static_assert(sizeof(To) == sizeof(From), "bitcast size");
+    To t;
+    memcpy(&t, &f, sizeof(To));
+    return t;
+}
+
+// ---- vector loads and stores (L1 bypass: every byte is touched once) -------
+
+template <int W>
+__device__ __forceinline__ Words<W> load_words(const char* p);
+
+template <>
+__device__ __forceinline__ Words<4> load_words<4>(const char* p)
+{
+    Words<4> r;
+    asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "l"(p));
+    return r;
+}
+template <>
+__device__ __forceinline__ Words<2> load_words<2>(const char* p)
+{
+    Words<2> r;
+    asm("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
+    return r;
+}
+template <>
+__device__ __forceinline__ Words<1> load_words<1>(const char* p)
+{
+    Words<1> r;
+    asm("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+    return r;
+}
+
+template <int W>
+__device__ __forceinline__ void store_words(char* p, const Words<W>& v);
+
+template <>
+__device__ __forceinline__ void store_words<4>(char* p, const Words<4>& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]) : "memory");
+}
+template <>
+__device__ __forceinline__ void store_words<2>(char* p, const Words<2>& v)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(v.w[0]), "r"(v.w[1]) : "memory");
+}
+template <>
+__device__ __forceinline__ void store_words<1>(char* p, const Words<1>& v)
+{
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(v.w[0]) : "memory");
+}
+
+// Copy units of VB bytes for the pure data-movement kernels (VB = 2: one
+// 16-bit element).
+struct Elem16 {
+    uint16_t h;
+};
+template <int VB>
+struct Chunk {
+    using type = Words<VB / 4>;
+    static __device__ __forceinline__ type load(const char* p) { return load_words<VB / 4>(p); }
+    static __device__ __forceinline__ void store(char* p, const type& v) { store_words<VB / 4>(p, v); }
+};
+template <>
+struct Chunk<2> {
+    using type = Elem16;
+    static __device__ __forceinline__ type load(const char* p)
+    {
+        Elem16 r;
+        asm("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(r.h) : "l"(p));
+        return r;
+    }
+    static __device__ __forceinline__ void store(char* p, const type& v)
+    {
+        asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(v.h) : "memory");
+    }
+};
+
+// ---- vector accumulators ----------------------------------------------------
+// init(x): acc = x (the root's vector); add(x): acc = acc (+) x; out(): encode.
+
+template <class T, int OP, int W>
+struct VecAcc;
+
+template <int OP, int W>
+struct VecAcc<float, OP, W> {
+    float a[W];
+    __device__ __forceinline__ void init(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] = __uint_as_float(x.w[i]);
+    }
+    __device__ __forceinline__ void add(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const float v = __uint_as_float(x.w[i]);
+            if constexpr (OP == kSum) a[i] = __fadd_rn(a[i], v);
+            else if constexpr (OP == kMax) a[i] = (v > a[i]) ? v : a[i];
+            else a[i] = (v < a[i]) ? v : a[i];
+        }
+    }
+    __device__ __forceinline__ Words<W> out() const
+    {
+        Words<W> r;
+#pragma unroll
+        for (int i = 0; i < W; ++i) r.w[i] = __float_as_uint(a[i]);
+        return r;
+    }
+};
+
+template <int OP, int W>
+struct VecAcc<int32_t, OP, W> {
+    uint32_t a[W];
+    __device__ __forceinline__ void init(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] = x.w[i];
+    }
+    __device__ __forceinline__ void add(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            if constexpr (OP == kSum) a[i] = a[i] + x.w[i];   // wraps modulo 2^32
+            else if constexpr (OP == kMax) a[i] = ((int32_t)x.w[i] > (int32_t)a[i]) ? x.w[i] : a[i];
+            else a[i] = ((int32_t)x.w[i] < (int32_t)a[i]) ? x.w[i] : a[i];
+        }
+    }
+    __device__ __forceinline__ Words<W> out() const
+    {
+        Words<W> r;
+#pragma unroll
+        for (int i = 0; i < W; ++i) r.w[i] = a[i];
+        return r;
+    }
+};
+
+// 16-bit Sum: each word holds two elements (low half = lower address);
+// widened exactly to binary32, accumulated there, narrowed with RNE.
+template <class T>
+struct Pair16;
+template <>
+struct Pair16<__half> {
+    using P = __half2;
+    static __device__ __forceinline__ float2 widen(uint32_t w) { return __half22float2(bitcast<__half2>(w)); }
+    static __device__ __forceinline__ uint32_t narrow(float lo, float hi)
+    {
+        return bitcast<uint32_t>(__floats2half2_rn(lo, hi));
+    }
+    static __device__ __forceinline__ uint32_t gt_mask(uint32_t x, uint32_t a)
+    {
+        return __hgt2_mask(bitcast<__half2>(x), bitcast<__half2>(a));
+    }
+    static __device__ __forceinline__ uint32_t lt_mask(uint32_t x, uint32_t a)
+    {
+        return __hlt2_mask(bitcast<__half2>(x), bitcast<__half2>(a));
+    }
+};
+template <>
+struct Pair16<__nv_bfloat16> {
+    using P = __nv_bfloat162;
+    static __device__ __forceinline__ float2 widen(uint32_t w) { return __bfloat1622float2(bitcast<__nv_bfloat162>(w)); }
+    static __device__ __forceinline__ uint32_t narrow(float lo, float hi)
+    {
+        return bitcast<uint32_t>(__floats2bfloat162_rn(lo, hi));
+    }
+    static __device__ __forceinline__ uint32_t gt_mask(uint32_t x, uint32_t a)
+    {
+        return __hgt2_mask(bitcast<__nv_bfloat162>(x), bitcast<__nv_bfloat162>(a));
+    }
+    static __device__ __forceinline__ uint32_t lt_mask(uint32_t x, uint32_t a)
+    {
+        return __hlt2_mask(bitcast<__nv_bfloat162>(x), bitcast<__nv_bfloat162>(a));
+    }
+};
+
+template <class T, int W>
+struct Acc16Sum {
+    float a[2 * W];
+    __device__ __forceinline__ void init(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const float2 f = Pair16<T>::widen(x.w[i]);
+            a[2 * i] = f.x;
+            a[2 * i + 1] = f.y;
+        }
+    }
+    __device__ __forceinline__ void add(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const float2 f = Pair16<T>::widen(x.w[i]);
+            a[2 * i] = __fadd_rn(a[2 * i], f.x);
+            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], f.y);
+        }
+    }
+    __device__ __forceinline__ Words<W> out() const
+    {
+        Words<W> r;
+#pragma unroll
+        for (int i = 0; i < W; ++i) r.w[i] = Pair16<T>::narrow(a[2 * i], a[2 * i + 1]);
+        return r;
+    }
+};
+
+// 16-bit Max / Min: an IEEE comparison per lane (false on NaN), then a
+// bitwise select of the raw encodings: x replaces acc only where strictly
+// greater (smaller).
+template <class T, int OP, int W>
+struct Acc16Sel {
+    uint32_t a[W];
+    __device__ __forceinline__ void init(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] = x.w[i];
+    }
+    __device__ __forceinline__ void add(const Words<W>& x)
+    {
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const uint32_t m = (OP == kMax) ? Pair16<T>::gt_mask(x.w[i], a[i])
+                                            : Pair16<T>::lt_mask(x.w[i], a[i]);
+            a[i] = (x.w[i] & m) | (a[i] & ~m);
+        }
+    }
+    __device__ __forceinline__ Words<W> out() const
+    {
+        Words<W> r;
+#pragma unroll
+        for (int i = 0; i < W; ++i) r.w[i] = a[i];
+        return r;
+    }
+};
+
+template <int W> struct VecAcc<__half, kSum, W> : Acc16Sum<__half, W> {};
+template <int W> struct VecAcc<__half, kMax, W> : Acc16Sel<__half, kMax, W> {};
+template <int W> struct VecAcc<__half, kMin, W> : Acc16Sel<__half, kMin, W> {};
+template <int W> struct VecAcc<__nv_bfloat16, kSum, W> : Acc16Sum<__nv_bfloat16, W> {};
+template <int W> struct VecAcc<__nv_bfloat16, kMax, W> : Acc16Sel<__nv_bfloat16, kMax, W> {};
+template <int W> struct VecAcc<__nv_bfloat16, kMin, W> : Acc16Sel<__nv_bfloat16, kMin, W> {};
+
+// ---- one element at a time (row tails, 2-byte-aligned buffers) ------------
+
+template <class T>
+struct Scalar;
+template <>
+struct Scalar<float> {
+    using Raw = uint32_t;
+};
+template <>
+struct Scalar<int32_t> {
+    using Raw = uint32_t;
+};
+template <>
+struct Scalar<__half> {
+    using Raw = uint16_t;
+    static __device__ __forceinline__ float widen(uint16_t h) { return __half2float(bitcast<__half>(h)); }
+    static __device__ __forceinline__ uint16_t narrow(float f) { return bitcast<uint16_t>(__float2half_rn(f)); }
+};
+template <>
+struct Scalar<__nv_bfloat16> {
+    using Raw = uint16_t;
+    static __device__ __forceinline__ float widen(uint16_t h) { return __bfloat162float(bitcast<__nv_bfloat16>(h)); }
+    static __device__ __forceinline__ uint16_t narrow(float f) { return bitcast<uint16_t>(__float2bfloat16_rn(f)); }
+};
+
+// Element `e` (offset in elements) of the reduction over src[0..n-1].
+template <class T, int OP>
+__device__ __forceinline__ typename Scalar<T>::Raw reduce_one(const ReduceParams& p, int64_t e)
+{
+    using Raw = typename Scalar<T>::Raw;
+    const int n = p.nranks;
+    Raw acc = reinterpret_cast<const Raw*>(p.src[0])[e];
+    if constexpr (std::is_same<T, float>::value) {
+        float a = __uint_as_float(acc);
+        for (int r = 1; r < n; ++r) {
+            const float v = __uint_as_float(reinterpret_cast<const Raw*>(p.src[r])[e]);
+            if constexpr (OP == kSum) a = __fadd_rn(a, v);
+            else if constexpr (OP == kMax) a = (v > a) ? v : a;
+            else a = (v < a) ? v : a;
+        }
+        return __float_as_uint(a);
+    } else if constexpr (std::is_same<T, int32_t>::value) {
+        for (int r = 1; r < n; ++r) {
+            const uint32_t v = reinterpret_cast<const Raw*>(p.src[r])[e];
+            if constexpr (OP == kSum) acc = acc + v;
+            else if constexpr (OP == kMax) acc = ((int32_t)v > (int32_t)acc) ? v : acc;
+            else acc = ((int32_t)v < (int32_t)acc) ? v : acc;
+        }
+        return acc;
+    } else {
+        float a = Scalar<T>::widen(acc);
+        for (int r = 1; r < n; ++r) {
+            const Raw raw = reinterpret_cast<const Raw*>(p.src[r])[e];
+            const float v = Scalar<T>::widen(raw);
+            if constexpr (OP == kSum) {
+                a = __fadd_rn(a, v);
+            } else if ((OP == kMax && v > a) || (OP == kMin && v < a)) {
+                a = v;
+                acc = raw;
+            }
+        }
+        if constexpr (OP == kSum) return Scalar<T>::narrow(a);
+        return acc;
+    }
+}
+
+// Rank that owns row `row` under the balanced bounds floor(r * rows / n):
+// the largest r with floor(r * rows / n) <= row, i.e. ((row + 1) n - 1) / rows.
+__device__ __forceinline__ int row_owner(int64_t row, int n, int64_t rows)
+{
+    return (int)(((row + 1) * (int64_t)n - 1) / rows);
+}
+
+// ---- the kernel --------------------------------------------------------------
+
+template <class T, int OP, int VB, int U>
+__device__ __forceinline__ void reduce_vectors(const ReduceParams& p)
+{
+    constexpr int W = VB / 4;
+    constexpr int VE = VB / (int)sizeof(T);        // elements per vector
+    constexpr int TV = kBlock * U;                 // vectors per tile
+    const int n = p.nranks;
+
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const int64_t row = t / p.tpr;
+        const int64_t seg = t - row * p.tpr;
+        const int64_t row_elem = row * p.ld;
+        char* dst_base = (char*)(p.scatter ? p.dst[row_owner(row, n, p.rows)] : p.dst[0]);
+        const int64_t v0 = seg * TV + threadIdx.x;
+
+        // byte offsets of this thread's U vectors (negative = inactive)
+        int64_t off[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t v = v0 + (int64_t)k * kBlock;
+            off[k] = (v < p.vpr) ? (row_elem * (int64_t)sizeof(T) + v * VB) : -1;
+        }
+
+        VecAcc<T, OP, W> acc[U];
+        {
+            Words<W> x[kGroup][U];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (j < n && off[k] >= 0) x[j][k] = load_words<W>((const char*)p.src[j] + off[k]);
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+                if (off[k] >= 0) acc[k].init(x[0][k]);
+#pragma unroll
+            for (int j = 1; j < kGroup; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (j < n && off[k] >= 0) acc[k].add(x[j][k]);
+        }
+        for (int g0 = kGroup; g0 < n; g0 += kGroup) {
+            Words<W> x[kGroup][U];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (g0 + j < n && off[k] >= 0) x[j][k] = load_words<W>((const char*)p.src[g0 + j] + off[k]);
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (g0 + j < n && off[k] >= 0) acc[k].add(x[j][k]);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (off[k] >= 0) store_words<W>(dst_base + off[k], acc[k].out());
+
+        // trailing elements of the row (fewer than one vector), owned by the
+        // row's last segment
+        if (p.tail > 0 && seg == p.tpr - 1) {
+            using Raw = typename Scalar<T>::Raw;
+            for (int c = threadIdx.x; c < p.tail; c += kBlock) {
+                const int64_t e = row_elem + p.vpr * VE + c;
+                reinterpret_cast<Raw*>(dst_base)[e] = reduce_one<T, OP>(p, e);
+            }
+        }
+    }
+}
+
+// One element per thread-slot: 16-bit data that is only 2-byte aligned.
+template <class T, int OP, int U>
+__device__ __forceinline__ void reduce_elements(const ReduceParams& p)
+{
+    using Raw = typename Scalar<T>::Raw;
+    constexpr int TV = kBlock * U;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const int64_t row = t / p.tpr;
+        const int64_t seg = t - row * p.tpr;
+        Raw* dst_base = (Raw*)(p.scatter ? p.dst[row_owner(row, p.nranks, p.rows)] : p.dst[0]);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t v = seg * TV + threadIdx.x + (int64_t)k * kBlock;
+            if (v < p.vpr) {
+                const int64_t e = row * p.ld + v;
+                dst_base[e] = reduce_one<T, OP>(p, e);
+            }
+        }
+    }
+}
+
+template <class T, int OP, int VB, int U>
+__global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ ReduceParams p)
+{
+    if constexpr (VB < 4) {
+        reduce_elements<T, OP, U>(p);
+    } else {
+        reduce_vectors<T, OP, VB, U>(p);
+    }
+}
+
+template <class T, int OP, int VB>
+cudaError_t launch_reduce_vb(const ReduceParams& p, int unroll, dim3 grid, cudaStream_t s)
+{
+    if (unroll == 2) reduce_kernel<T, OP, VB, 2><<<grid, kBlock, 0, s>>>(p);
+    else reduce_kernel<T, OP, VB, 1><<<grid, kBlock, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <class T, int OP>
+cudaError_t launch_reduce_op(const ReduceParams& p, int vb, int unroll, dim3 grid, cudaStream_t s)
+{
+    switch (vb) {
+    case 16: return launch_reduce_vb<T, OP, 16>(p, unroll, grid, s);
+    case 8: return launch_reduce_vb<T, OP, 8>(p, unroll, grid, s);
+    case 4: return launch_reduce_vb<T, OP, 4>(p, unroll, grid, s);
+    default:
+        if constexpr (sizeof(T) == 2) return launch_reduce_vb<T, OP, 2>(p, unroll, grid, s);
+        return cudaErrorInvalidValue;
+    }
+}
+
+template <class T>
+cudaError_t launch_reduce_t(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s)
+{
+    switch (op) {
+    case kSum: return launch_reduce_op<T, kSum>(p, vb, unroll, grid, s);
+    case kMax: return launch_reduce_op<T, kMax>(p, vb, unroll, grid, s);
+    default: return launch_reduce_op<T, kMin>(p, vb, unroll, grid, s);
+    }
+}
+
+template <class T, int OP, int VB, int U>
+int occupancy_of()
+{
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reduce_kernel<T, OP, VB, U>, kBlock, 0) != cudaSuccess)
+        return 1;
+    return b > 0 ? b : 1;
+}
+
+template <class T>
+int occupancy_t(int op, int vb, int unroll)
+{
+#define PTOC_OCC(OPV)                                                                   \
+    if (vb == 16) return unroll == 2 ? occupancy_of<T, OPV, 16, 2>() : occupancy_of<T, OPV, 16, 1>(); \
+    if (vb == 8) return unroll == 2 ? occupancy_of<T, OPV, 8, 2>() : occupancy_of<T, OPV, 8, 1>();    \
+    return unroll == 2 ? occupancy_of<T, OPV, 4, 2>() : occupancy_of<T, OPV, 4, 1>();
+    if (op == kSum) { PTOC_OCC(kSum) }
+    if (op == kMax) { PTOC_OCC(kMax) }
+    PTOC_OCC(kMin)
+#undef PTOC_OCC
+}
+
+}  // namespace ptoc
