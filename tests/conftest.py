@@ -15,8 +15,8 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     # The library, the oracle and the generator are built in-tree (nvcc / gcc)
     # before collection, so test modules can import them.
-    from tile_level_collective_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import oracle
     import synth
     oracle.build()

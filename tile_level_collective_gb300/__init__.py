@@ -32,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libptoc.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         "libptoc.so is not built (expected at %s); build it with "
-        "`python -m tile_level_collective_gb300._build` or __graft_entry__.build()" % LIB_PATH)
+        "`python tile_level_collective_gb300/_build.py` or __graft_entry__.build()" % LIB_PATH)
 
 _lib = ctypes.CDLL(LIB_PATH)
 

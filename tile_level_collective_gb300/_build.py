@@ -3,7 +3,7 @@
 Each .cu under csrc/ is compiled by nvcc in parallel into _build/, then linked
 into tile_level_collective_gb300/libptoc.so. No fast-math, no FMA contraction
 concerns (the kernels add, compare and select only). Run as
-``python -m tile_level_collective_gb300._build`` or through
+``python tile_level_collective_gb300/_build.py`` or through
 ``__graft_entry__.build()``.
 """
 import glob
