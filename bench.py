@@ -8,9 +8,11 @@ valid box inside NaN-sentinel padding, N(0, 1) values; one step = Sum, Max and
 Min (three launches). Metric: effective HBM GB/s = (N + 1) * bytes/elem *
 valid elements per launch, summed over the step, divided by the step's device
 time. Inputs are generated on the host by the seeded generator and resident in
-HBM before timing; L2 is flushed (a 256 MiB write, outside the timed events)
-before every step. Other workloads (the parity configurations) can be timed
-with --workload for the per-kernel evidence.
+HBM before timing; before every step L2 is flushed outside the timed events
+(a 256 MiB write, then a 256 MiB read of another buffer, so that no dirty
+flush lines are left for the timed kernels to write back). Other workloads
+(the parity configurations) can be timed with --workload for the per-kernel
+evidence.
 
 --impl reference times the CPU oracle on this machine's host cores (the only
 other implementation there is), on a bounded sample of the same workload per
@@ -33,10 +35,27 @@ sys.path.insert(0, ROOT)
 METRIC = "TREDUCE effective HBM GB/s (N reads + 1 write) and % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["tile_level_collective_gb300/csrc/reduce_impl.cuh",
-                  "tile_level_collective_gb300/csrc/movement.cu",
-                  "tile_level_collective_gb300/csrc/ptoc_api.cu",
-                  "tile_level_collective_gb300/csrc/ptoc_internal.h"]
+
+
+L2_NOTE = ("flushed before every step, outside the timed events: 256 MiB write, then 256 MiB read "
+           "of another buffer (cold, clean L2)")
+
+
+class L2Flush:
+    """Leaves L2 cold and clean: writes one buffer larger than L2, then reads
+    another one, which evicts (writes back) the dirty lines of the first."""
+
+    def __init__(self, dev):
+        import torch
+        self.a = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.b = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int32, device=dev)
+
+    def __call__(self, k=0):
+        import torch
+        self.a.fill_(k & 0xFF)
+        torch.amax(self.b, dim=0, out=self.sink)
+KERNEL_SOURCE_DIRS = ["tile_level_collective_gb300/csrc", "include"]
 
 
 # ---------------------------------------------------------------------------
@@ -122,7 +141,7 @@ class TreduceBench(Workload):
                 "seed": "1234 + rank (SplitMix64, counter-based)",
                 "step": "%d TREDUCE launches (%s)" % (len(w.ops), ", ".join(w.ops)),
                 "bytes_per_step": self.bytes_per_step(),
-                "l2": "flushed before every step (256 MiB device write, outside the timed events)"}
+                "l2": L2_NOTE}
 
     # oracle on a bounded sample: the first `rows` rows of the valid box
     def oracle_sample(self, rows):
@@ -172,7 +191,7 @@ class RsAgBench(Workload):
 
     def setup_host(self):
         import synth
-        self.host = [synth.window(r) for r in range(self.cfg["nranks"])]
+        self.host = [synth.window(r, self.cfg) for r in range(self.cfg["nranks"])]
 
     def setup_device(self, dev):
         self.dev = [_to_dev(h, dev) for h in self.host]
@@ -212,7 +231,7 @@ class RsAgBench(Workload):
                 "storage_dtype": "f16", "shape": [c["rows"], c["cols"]], "ld": c["ld"],
                 "values": "normal(0,1)", "step": "reduce_scatter (Sum) then allgather",
                 "bytes_per_step": self.bytes_per_step(),
-                "l2": "flushed before every step (256 MiB device write, outside the timed events)"}
+                "l2": L2_NOTE}
 
     def oracle_sample(self, rows):
         import numpy as np
@@ -305,7 +324,7 @@ class A2avBench(Workload):
                 "row_elems": c["size"], "target_rows": c["target_rows"], "max_recv": self.mr,
                 "send_counts": "uniform int [0, 2047] per (src, dest), seed 1234 + src",
                 "moved_rows": self.moved_rows, "bytes_per_step": self.bytes_per_step(),
-                "l2": "flushed before every step (256 MiB device write, outside the timed events)"}
+                "l2": L2_NOTE}
 
     def oracle_sample(self, rows):
         import numpy as np
@@ -330,21 +349,37 @@ class A2avBench(Workload):
         return 16.0 / max(dt, 1e-9)
 
 
-def make_workload(name):
+def make_workload(name, rows_div=1):
+    """The named workload; rows_div > 1 divides its row counts (a smaller case
+    of the same kernel, for profiler captures)."""
     import synth
+    wl = None
     if name in ("treduce", "treduce_bf16"):
-        return TreduceBench(synth.config2(), "bf16")
-    if name == "treduce_small":
-        return TreduceBench(synth.config1(), "f32")
-    if name == "treduce_f32":
-        return TreduceBench(synth.config3(), "f32")
-    if name == "treduce_i32":
-        return TreduceBench(synth.config3_int(), "i32")
-    if name == "rs_ag":
-        return RsAgBench()
-    if name == "a2av":
-        return A2avBench()
-    raise SystemExit("unknown workload %s" % name)
+        wl = TreduceBench(synth.config2(), "bf16")
+    elif name == "treduce_small":
+        wl = TreduceBench(synth.config1(), "f32")
+    elif name == "treduce_f32":
+        wl = TreduceBench(synth.config3(), "f32")
+    elif name == "treduce_i32":
+        wl = TreduceBench(synth.config3_int(), "i32")
+    elif name == "rs_ag":
+        wl = RsAgBench()
+    elif name == "a2av":
+        wl = A2avBench()
+    else:
+        raise SystemExit("unknown workload %s" % name)
+    if rows_div > 1:
+        if isinstance(wl, TreduceBench):
+            w = wl.w
+            w.rows, w.valid_rows = w.rows // rows_div, w.valid_rows // rows_div
+            w.name += "_rows_div%d" % rows_div
+            wl.name = w.name
+        else:
+            wl.cfg = dict(wl.cfg)
+            key = "rows" if isinstance(wl, RsAgBench) else "target_rows"
+            wl.cfg[key] = wl.cfg[key] // rows_div
+            wl.name += "_rows_div%d" % rows_div
+    return wl
 
 
 # ---------------------------------------------------------------------------
@@ -385,10 +420,15 @@ def measured_peak():
 
 
 def kernel_source_hash():
+    """Hash of every library source file (kernels, launch code, header)."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    for d in KERNEL_SOURCE_DIRS:
+        for name in sorted(os.listdir(os.path.join(ROOT, d))):
+            path = os.path.join(ROOT, d, name)
+            if os.path.isfile(path) and name.endswith((".cu", ".cuh", ".h")):
+                h.update(name.encode())
+                with open(path, "rb") as f:
+                    h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -476,6 +516,13 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def aggregate(ms_local, bytes_per_step, world, device):
+    """Whole-job figures of a replica run: the step time is the max over ranks
+    and `value` counts the bytes every rank processed (weak scaling)."""
+    ms = max_over_ranks(ms_local, world, device)
+    return ms, world * bytes_per_step / (ms / 1e3) / 1e9
+
+
 def cpu_baseline(wl, budget_s):
     """The oracle as it stands, single-threaded, on a sample of the workload
     (at most the whole step), repeated to about `budget_s` seconds of CPU
@@ -504,15 +551,15 @@ def run_ours(args):
             import torch.distributed as dist
             dist.barrier()
 
-    wl = make_workload(args.workload)
+    wl = make_workload(args.workload, args.rows_div)
     wl.setup_host()
     wl.setup_device(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     nl = wl.launches_per_step()
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         for i in range(nl):
             wl.launch(i)
     torch.cuda.synchronize()
@@ -526,7 +573,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
-        flush.fill_(k & 0xFF)
+        flush(k)
         for i in range(nl):
             ev[k][i][0].record(stream)
             wl.launch(i)
@@ -540,8 +587,7 @@ def run_ours(args):
     # a step = its launches back to back on the stream (the flush between steps excluded)
     step_ms = [sum(x) for x in per_launch]
     ms_local = sum(step_ms) / args.steps
-    ms = max_over_ranks(ms_local, world, dev)
-    value = world * wl.bytes_per_step() / (ms / 1e3) / 1e9
+    ms, value = aggregate(ms_local, wl.bytes_per_step(), world, dev)
 
     # roofline of the dominant kernel: launch 0's family
     avg0 = statistics.mean(x[0] for x in per_launch) if nl == 1 or args.workload == "rs_ag" else \
@@ -551,6 +597,21 @@ def run_ours(args):
     traffic = recorded_traffic(wl.name)
 
     # end to end: pinned host inputs in, results out, every step
+    if args.no_e2e:
+        e_ms, e_value = None, None
+    else:
+        e_ms, e_value = run_e2e(wl, args, dev, stream, world, barrier)
+    if rank != 0:
+        return
+    line = build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl,
+                      sampler.summary(t0, t1) if sampler else None)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(wl, args, dev, stream, world, barrier):
+    import torch
     wl.setup_e2e(dev)
     for _ in range(max(1, min(args.warmup, 3))):
         wl.e2e_step()
@@ -564,11 +625,10 @@ def run_ours(args):
         wl.e2e_step()
     ee.record(stream)
     torch.cuda.synchronize()
-    e_ms = max_over_ranks(es.elapsed_time(ee) / e_steps, world, dev)
-    e_value = world * wl.bytes_per_step() / (e_ms / 1e3) / 1e9
+    return aggregate(es.elapsed_time(ee) / e_steps, wl.bytes_per_step(), world, dev)
 
-    if rank != 0:
-        return
+
+def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl, clocks):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
@@ -579,15 +639,14 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": wl.kernel,
                      "bytes_per_launch": wl.bytes_per_launch(), "avg_launch_ms": round(avg0, 6),
                      "peak_source": peak_src},
-        "e2e": {"value": round(e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes(),
-                "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": round(e_ms, 6),
-                "path": "pinned host -> device copy, the library calls, device -> pinned host copy"},
+        "e2e": None if e_value is None else {
+            "value": round(e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes(),
+            "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": round(e_ms, 6),
+            "path": "pinned host -> device copy, the library calls, device -> pinned host copy"},
         "gpu_launches": nl * args.steps,
-        "clocks": sampler.summary(t0, t1) if sampler else None,
+        "clocks": clocks,
     }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_reference(args):
@@ -595,7 +654,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    wl = make_workload(args.workload)
+    wl = make_workload(args.workload, args.rows_div)
     wl.setup_host()
     total_steps = args.steps + args.warmup
     per_step = max(0.002, args.reference_seconds / max(1, total_steps))
@@ -635,6 +694,9 @@ def parse(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiler runs)")
+    ap.add_argument("--rows-div", type=int, default=1,
+                    help="divide the workload's rows (a smaller case for profiler captures)")
     return ap.parse_args(argv)
 
 

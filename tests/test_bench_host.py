@@ -1,0 +1,66 @@
+"""Host-side logic of the multi-GPU benchmark, on CPU: world-size-2 gloo ranks
+run bench.aggregate (max step time over ranks, whole-job value), the argument
+parser keeps the driver's defaults, and the reference arm's JSON line has the
+keys the contract asks for."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, results):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms_local = [2.0, 5.0][rank]          # rank 1 is the slow one
+    ms, value = bench.aggregate(ms_local, 1_000_000_000, world, torch.device("cpu"))
+    results[rank] = (ms, value)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_aggregate_max_over_two_gloo_ranks():
+    world, port = 2, _free_port()
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_rank_main, args=(world, port, results), nprocs=world, join=True)
+        got = dict(results)
+    for rank in range(world):
+        ms, value = got[rank]
+        assert ms == 5.0                              # the max over ranks
+        assert abs(value - 2 * 1e9 / 5e-3 / 1e9) < 1e-6  # both ranks' bytes / max time
+
+
+def test_defaults_and_reference_line():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = bench.parse([])
+    assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours" and a.workload == "treduce"
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "1", "--reference-seconds", "1",
+                          "--workload", "treduce_small"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert key in line
+    assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0

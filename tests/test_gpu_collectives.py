@@ -194,3 +194,23 @@ def test_workload_5_all_to_all_v_full():
                 blk = got[s * mr:s * mr + c, :3]
                 assert np.all(blk[:, 0] == s) and np.all(blk[:, 1] == d)
                 assert np.array_equal(blk[:, 2], np.arange(c, dtype=np.uint16))
+
+
+@pytest.mark.parametrize("variant", ["vec", "async"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_scatter_both_kernels(variant, dtype, monkeypatch):
+    monkeypatch.setenv("PTOC_VARIANT", variant)
+    n, rows, cols, ld = 9, 20, 136, 136
+    host = windows_host(dtype, n, rows, cols, ld, seed=21)
+    dev = [DevBuf(h) for h in host]
+    P.ptoc_reduce_scatter([d.ptr for d in dev], rows, cols, ld, P.SUM, PCODE[dtype])
+    torch.cuda.synchronize()
+    oracle.reduce_scatter(host, rows, cols, ld, oracle.SUM, ORC_DT[dtype])
+    for r in range(n):
+        assert nan_equal(dev[r].host(), host[r], dtype) and dev[r].guards_intact()
+
+
+@pytest.mark.parametrize("unroll", ["4", "8"])
+def test_all_to_all_v_both_unrolls(unroll, monkeypatch):
+    monkeypatch.setenv("PTOC_A2AV_UNROLL", unroll)
+    run_a2av(6, 600, 520, np.uint16, -5, 110, seed=33)

@@ -85,19 +85,19 @@ cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 gr
 // all_to_all_v
 // ---------------------------------------------------------------------------
 
-constexpr int kA2avUnroll = 4;     // vectors per thread per tile
-
-__device__ __forceinline__ int64_t clamp_count(int32_t c, int64_t max_recv)
+__device__ __forceinline__ int32_t clamp_count(int32_t c, int64_t max_recv)
 {
     int64_t v = c;
     v = v < 0 ? 0 : v;
-    return v > max_recv ? max_recv : v;
+    return (int32_t)(v > max_recv ? max_recv : v);
 }
 
-// Exclusive prefix over pairs: pre[q] = tiles of pairs 0..q-1, pre[np] = total.
-// Each thread scans a contiguous run of pairs; the run totals are combined with
-// a warp-shuffle scan and a second pass over the warp totals.
-__device__ void build_tile_prefix(const A2avParams& p, int64_t* pre, int64_t* warp_tot)
+// Per-pair state in shared memory: cnt[q] = clamped count of pair q
+// (q = s * N + d), pre[q] = tiles of pairs 0..q-1 (exclusive prefix), pre[np]
+// = total. Each thread scans a contiguous run of pairs; the run totals are
+// combined with a warp-shuffle scan and a pass over the warp totals. Block 0
+// also publishes the counts to recv_counts.
+__device__ void build_pairs(const A2avParams& p, int32_t* cnt, int32_t* pre, int32_t* warp_tot)
 {
     const int n = p.nranks;
     const int np = n * n;
@@ -105,58 +105,60 @@ __device__ void build_tile_prefix(const A2avParams& p, int64_t* pre, int64_t* wa
     const int q0 = threadIdx.x * per;
     const int q1 = min(q0 + per, np);
 
-    int64_t run = 0;
+    int32_t run = 0;
     for (int q = q0; q < q1; ++q) {
         const int s = q / n, d = q - (q / n) * n;
-        const int64_t c = clamp_count(p.sc[s][d], p.max_recv);
-        if (blockIdx.x == 0) p.rc[d][s] = (int32_t)c;
-        const int64_t tiles = (c * p.row_bytes + p.tile_bytes - 1) / p.tile_bytes;
+        const int32_t c = clamp_count(p.sc[s][d], p.max_recv);
+        if (blockIdx.x == 0) p.rc[d][s] = c;
+        cnt[q] = c;
+        const int32_t tiles = (int32_t)(((int64_t)c * p.row_bytes + p.tile_bytes - 1) / p.tile_bytes);
         pre[q] = tiles;                 // temporarily: this pair's tile count
         run += tiles;
     }
 
-    // inclusive scan of the per-thread run totals
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int64_t incl = run;
+    int32_t incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (threadIdx.x == 0) {
-        int64_t acc = 0;
+        int32_t acc = 0;
         for (int w = 0; w < kBlock / 32; ++w) {
-            const int64_t t = warp_tot[w];
+            const int32_t t = warp_tot[w];
             warp_tot[w] = acc;
             acc += t;
         }
         pre[np] = acc;
     }
     __syncthreads();
-    int64_t excl = warp_tot[warp] + incl - run;   // tiles before this thread's run
+    int32_t excl = warp_tot[warp] + incl - run;   // tiles before this thread's run
     for (int q = q0; q < q1; ++q) {
-        const int64_t tiles = pre[q];
+        const int32_t tiles = pre[q];
         pre[q] = excl;
         excl += tiles;
     }
     __syncthreads();
 }
 
-template <int VB>
+// U chunks of VB bytes per thread per tile: tile_bytes = U * kBlock * VB.
+template <int VB, int U>
 __global__ void __launch_bounds__(kBlock) a2av_kernel(const __grid_constant__ A2avParams p)
 {
-    extern __shared__ int64_t smem[];
-    __shared__ int64_t warp_tot[kBlock / 32];
+    extern __shared__ int32_t smem[];
+    __shared__ int32_t warp_tot[kBlock / 32];
     using C = Chunk<VB>;
     const int n = p.nranks;
     const int np = n * n;
-    int64_t* pre = smem;                    // np + 1 entries
-    build_tile_prefix(p, pre, warp_tot);
-    const int64_t total = pre[np];
+    int32_t* cnt = smem;                    // np entries
+    int32_t* pre = smem + np;               // np + 1 entries
+    build_pairs(p, cnt, pre, warp_tot);
+    const int32_t total = pre[np];
 
-    for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int32_t t = blockIdx.x; t < total; t += gridDim.x) {
         // the pair q with pre[q] <= t < pre[q + 1]
         int lo = 0, hi = np;                // invariant: pre[lo] <= t < pre[hi]
         while (hi - lo > 1) {
@@ -166,47 +168,59 @@ __global__ void __launch_bounds__(kBlock) a2av_kernel(const __grid_constant__ A2
         }
         const int q = lo;
         const int s = q / n, d = q - (q / n) * n;
-        const int64_t bytes = clamp_count(p.sc[s][d], p.max_recv) * p.row_bytes;
-        const int64_t beg = (t - pre[q]) * p.tile_bytes;
+        const int64_t bytes = (int64_t)cnt[q] * p.row_bytes;
+        const int64_t beg = (int64_t)(t - pre[q]) * p.tile_bytes;
         const int64_t len = min(p.tile_bytes, bytes - beg);
         const char* src = (const char*)p.in[s] + d * p.max_recv * p.row_bytes + beg;
         char* dst = (char*)p.tgt[d] + s * p.max_recv * p.row_bytes + beg;
 
-        typename C::type x[kA2avUnroll];
+        typename C::type x[U];
 #pragma unroll
-        for (int k = 0; k < kA2avUnroll; ++k) {
+        for (int k = 0; k < U; ++k) {
             const int64_t o = ((int64_t)k * kBlock + threadIdx.x) * VB;
             if (o < len) x[k] = C::load(src + o);
         }
 #pragma unroll
-        for (int k = 0; k < kA2avUnroll; ++k) {
+        for (int k = 0; k < U; ++k) {
             const int64_t o = ((int64_t)k * kBlock + threadIdx.x) * VB;
             if (o < len) C::store(dst + o, x[k]);
         }
     }
 }
 
-size_t a2av_smem_bytes(int nranks) { return (size_t)(nranks * nranks + 1) * sizeof(int64_t); }
+size_t a2av_smem_bytes(int nranks) { return (size_t)(2 * nranks * nranks + 1) * sizeof(int32_t); }
 
-cudaError_t launch_a2av(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
+template <int U>
+static cudaError_t launch_a2av_u(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
     const size_t smem = a2av_smem_bytes(p.nranks);
-    if (vb == 16) a2av_kernel<16><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 8) a2av_kernel<8><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 4) a2av_kernel<4><<<grid, kBlock, smem, s>>>(p);
-    else a2av_kernel<2><<<grid, kBlock, smem, s>>>(p);
+    if (vb == 16) a2av_kernel<16, U><<<grid, kBlock, smem, s>>>(p);
+    else if (vb == 8) a2av_kernel<8, U><<<grid, kBlock, smem, s>>>(p);
+    else if (vb == 4) a2av_kernel<4, U><<<grid, kBlock, smem, s>>>(p);
+    else a2av_kernel<2, U><<<grid, kBlock, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-int a2av_blocks_per_sm(int vb, int nranks)
+cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s)
+{
+    return unroll == 8 ? launch_a2av_u<8>(p, vb, grid, s) : launch_a2av_u<4>(p, vb, grid, s);
+}
+
+template <int U>
+static int a2av_occupancy_u(int vb, size_t smem)
 {
     int b = 0;
-    const size_t smem = a2av_smem_bytes(nranks);
-    cudaError_t e = vb == 16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<16>, kBlock, smem)
-                  : vb == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<8>, kBlock, smem)
-                  : vb == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<4>, kBlock, smem)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<2>, kBlock, smem);
+    cudaError_t e = vb == 16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<16, U>, kBlock, smem)
+                  : vb == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<8, U>, kBlock, smem)
+                  : vb == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<4, U>, kBlock, smem)
+                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<2, U>, kBlock, smem);
     return (e == cudaSuccess && b > 0) ? b : 1;
+}
+
+int a2av_blocks_per_sm(int vb, int unroll, int nranks)
+{
+    const size_t smem = a2av_smem_bytes(nranks);
+    return unroll == 8 ? a2av_occupancy_u<8>(vb, smem) : a2av_occupancy_u<4>(vb, smem);
 }
 
 }  // namespace ptoc

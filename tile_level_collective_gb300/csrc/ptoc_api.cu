@@ -62,20 +62,72 @@ int pick_vector_bytes(uintptr_t addr_or, int64_t pitch_bytes, int eb)
     return eb;
 }
 
-std::atomic<int> g_sm_count[64];
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    return dev;
+}
 
 int sm_count()
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-    if (dev < 64) {
+    const int dev = current_device();
+    if (dev < kMaxDevices) {
         int c = g_sm_count[dev].load(std::memory_order_relaxed);
         if (c > 0) return c;
     }
     int c = 1;
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 1;
-    if (dev < 64) g_sm_count[dev].store(c, std::memory_order_relaxed);
+    if (dev < kMaxDevices) g_sm_count[dev].store(c, std::memory_order_relaxed);
     return c;
+}
+
+// Optional A/B switch for measurements: PTOC_VARIANT=vec forces the register
+// kernel on 16-byte-aligned data (default: the shared-memory pipeline).
+bool use_async_variant()
+{
+    const char* e = getenv("PTOC_VARIANT");
+    return !(e && strcmp(e, "vec") == 0);
+}
+
+// Pipeline shape of the shared-memory kernel: PTOC_ASYNC_CFG=<index> into
+// the shape table (A/B switch for measurements; 0 is the default shape).
+int async_cfg()
+{
+    const char* e = getenv("PTOC_ASYNC_CFG");
+    if (e && e[0] >= '0' && e[0] < '0' + kAsyncCfgs && e[1] == 0) return e[0] - '0';
+    return 0;
+}
+
+// Chunks per thread per all_to_all_v tile: PTOC_A2AV_UNROLL=4|8 (A/B
+// switch for measurements; default 8).
+int a2av_unroll()
+{
+    const char* e = getenv("PTOC_A2AV_UNROLL");
+    return (e && strcmp(e, "4") == 0) ? 4 : 8;
+}
+
+int async_occupancy(int dtype, int op, int cfg)
+{
+    const int dev = current_device();
+    switch (dtype) {
+    case PTOC_F32: return occupancy_async_f32(op, cfg, dev);
+    case PTOC_I32: return occupancy_async_i32(op, cfg, dev);
+    case PTOC_F16: return occupancy_async_f16(op, cfg, dev);
+    default: return occupancy_async_bf16(op, cfg, dev);
+    }
+}
+
+cudaError_t launch_async(int dtype, const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s)
+{
+    switch (dtype) {
+    case PTOC_F32: return launch_async_f32(p, op, cfg, grid, s);
+    case PTOC_I32: return launch_async_i32(p, op, cfg, grid, s);
+    case PTOC_F16: return launch_async_f16(p, op, cfg, grid, s);
+    default: return launch_async_bf16(p, op, cfg, grid, s);
+    }
 }
 
 // Optional A/B switch for measurements: PTOC_UNROLL=1|2 (vectors per thread
@@ -118,8 +170,8 @@ dim3 grid_for(int64_t ntiles)
     return dim3((unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap));
 }
 
-cudaError_t launch_reduce(int dtype, const ReduceParams& p, int op, int vb, int unroll, dim3 grid,
-                          cudaStream_t s)
+cudaError_t launch_reduce_regs(int dtype, const ReduceParams& p, int op, int vb, int unroll, dim3 grid,
+                               cudaStream_t s)
 {
     switch (dtype) {
     case PTOC_F32: return launch_reduce_f32(p, op, vb, unroll, grid, s);
@@ -127,6 +179,38 @@ cudaError_t launch_reduce(int dtype, const ReduceParams& p, int op, int vb, int 
     case PTOC_F16: return launch_reduce_f16(p, op, vb, unroll, grid, s);
     default: return launch_reduce_bf16(p, op, vb, unroll, grid, s);
     }
+}
+
+// Tile a [rows, cols] box with pitch ld and launch one reduction over it
+// (p.src, p.dst, p.nranks and p.scatter already filled in): the
+// shared-memory pipeline when every address and the pitch are 16-byte
+// aligned, the register kernel otherwise.
+cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, int64_t cols, int64_t ld,
+                             int eb, int vb, cudaStream_t s)
+{
+    p.ld = ld;
+    p.rows = rows;
+    if (vb == 16 && use_async_variant()) {
+        const int cfg = async_cfg();
+        const int occ = async_occupancy(dtype, op, cfg);
+        if (occ > 0) {
+            const Box b = make_box(rows, cols, ld, eb, 16, kAsyncB[cfg]);
+            p.vpr = b.vpr;
+            p.tail = b.tail;
+            p.tpr = b.tpr;
+            p.ntiles = b.ntiles;
+            const int64_t want = (int64_t)sm_count() * occ;
+            const int grid = (int)(want < b.ntiles ? want : b.ntiles);
+            return launch_async(dtype, p, op, cfg, grid, s);
+        }
+    }
+    const int unroll = reduce_unroll(vb);
+    const Box b = make_box(rows, cols, ld, eb, vb, kBlock * unroll);
+    p.vpr = b.vpr;
+    p.tail = b.tail;
+    p.tpr = b.tpr;
+    p.ntiles = b.ntiles;
+    return launch_reduce_regs(dtype, p, op, vb, unroll, grid_for(p.ntiles), s);
 }
 
 ptoc_status check_group(const ptoc_group* g, bool need_root)
@@ -224,15 +308,7 @@ extern "C" ptoc_status ptoc_treduce(const ptoc_group* group, void* dst, int64_t 
     uintptr_t addr_or = (uintptr_t)dst;
     for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)group->tensors[r];
     const int vb = pick_vector_bytes(addr_or, flat ? 0 : ld * eb, eb);
-    const int unroll = reduce_unroll(vb);
-    const Box b = make_box(frows, fcols, fld, eb, vb, kBlock * unroll);
-    p.ld = b.ld;
-    p.rows = b.rows;
-    p.vpr = b.vpr;
-    p.tail = b.tail;
-    p.tpr = b.tpr;
-    p.ntiles = b.ntiles;
-    cudaError_t e = launch_reduce(dtype, p, eff_op, vb, unroll, grid_for(p.ntiles), stream);
+    cudaError_t e = launch_reduction(dtype, p, eff_op, frows, fcols, fld, eb, vb, stream);
     return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }
 
@@ -260,15 +336,7 @@ extern "C" ptoc_status ptoc_reduce_scatter(const ptoc_group* windows, int64_t ro
     uintptr_t addr_or = 0;
     for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)windows->tensors[r];
     const int vb = pick_vector_bytes(addr_or, ld * eb, eb);
-    const int unroll = reduce_unroll(vb);
-    const Box b = make_box(rows, cols, ld, eb, vb, kBlock * unroll);
-    p.ld = ld;
-    p.rows = rows;
-    p.vpr = b.vpr;
-    p.tail = b.tail;
-    p.tpr = b.tpr;
-    p.ntiles = b.ntiles;
-    cudaError_t e = launch_reduce(dtype, p, eff_op, vb, unroll, grid_for(p.ntiles), stream);
+    cudaError_t e = launch_reduction(dtype, p, eff_op, rows, cols, ld, eb, vb, stream);
     return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }
 
@@ -354,10 +422,13 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
     uintptr_t addr_or = 0;
     for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)inputs->tensors[r] | (uintptr_t)targets->tensors[r];
     const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
-    p.tile_bytes = (int64_t)vb * kBlock * 4;
-    const int per_sm = a2av_blocks_per_sm(vb, n);
+    const int unroll = a2av_unroll();
+    p.tile_bytes = (int64_t)vb * kBlock * unroll;
+    // tile indices are int32 in the kernel
+    if ((int64_t)n * fp / p.tile_bytes + (int64_t)n * n >= INT32_MAX) return PTOC_ERR_UNSUPPORTED;
+    const int per_sm = a2av_blocks_per_sm(vb, unroll, n);
     dim3 grid((unsigned)(sm_count() * per_sm));
-    cudaError_t e = launch_a2av(p, vb, grid, stream);
+    cudaError_t e = launch_a2av(p, vb, unroll, grid, stream);
     return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }
 

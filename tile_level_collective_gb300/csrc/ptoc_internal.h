@@ -12,8 +12,19 @@ namespace ptoc {
 
 constexpr int kMaxRanks = PTOC_MAX_RANKS;
 constexpr int kBlock = 256;          // threads per CTA for every streaming kernel
+constexpr int kMaxDevices = 64;      // per-device caches
 
 enum Op : int { kSum = 0, kMax = 1, kMin = 2 };
+
+// Shapes of the shared-memory-pipelined reduction: S stages of G ranks, CTAs
+// of B threads (one tile = B vectors of 16 bytes). Shared memory per CTA is
+// S * G * B * 16 bytes. Index 0 is the default; PTOC_ASYNC_CFG=<index>
+// selects another one for measurements.
+constexpr int kAsyncCfgs = 6;
+constexpr int kAsyncS[kAsyncCfgs] = {2, 3, 2, 3, 4, 2};
+constexpr int kAsyncG[kAsyncCfgs] = {8, 8, 8, 8, 4, 16};
+constexpr int kAsyncB[kAsyncCfgs] = {256, 256, 128, 128, 256, 256};
+constexpr size_t async_smem_bytes(int cfg) { return (size_t)kAsyncS[cfg] * kAsyncG[cfg] * kAsyncB[cfg] * 16; }
 
 // TREDUCE and reduce_scatter. The box is `rows` rows of `vpr` full vectors of
 // VB bytes plus `tail` trailing elements; one tile is one row segment of
@@ -39,7 +50,8 @@ struct GatherParams {
 };
 
 // all_to_all_v: one contiguous segment per (s, d) pair, cut into tiles of
-// tile_bytes; prefix sums over pairs are built in shared memory per CTA.
+// tile_bytes; clamped counts and tile prefix sums over pairs are built in
+// shared memory per CTA (int32: a launch moves fewer than 2^31 tiles).
 struct A2avParams {
     const void* in[kMaxRanks];
     void* tgt[kMaxRanks];
@@ -59,14 +71,24 @@ cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int vb, int unroll,
 cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s);
-cudaError_t launch_a2av(const A2avParams& p, int vb, dim3 grid, cudaStream_t s);
+cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s);
+
+// Shared-memory-pipelined reduction (16-byte-aligned data): persistent grid.
+cudaError_t launch_async_f32(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
+cudaError_t launch_async_i32(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
+cudaError_t launch_async_f16(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
+cudaError_t launch_async_bf16(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
+int occupancy_async_f32(int op, int cfg, int dev);
+int occupancy_async_i32(int op, int cfg, int dev);
+int occupancy_async_f16(int op, int cfg, int dev);
+int occupancy_async_bf16(int op, int cfg, int dev);
 
 // Resident CTAs per SM for each kernel (occupancy query).
 int occupancy_reduce_f32(int op, int vb, int unroll);
 int occupancy_reduce_i32(int op, int vb, int unroll);
 int occupancy_reduce_f16(int op, int vb, int unroll);
 int occupancy_reduce_bf16(int op, int vb, int unroll);
-int a2av_blocks_per_sm(int vb, int nranks);
+int a2av_blocks_per_sm(int vb, int unroll, int nranks);
 size_t a2av_smem_bytes(int nranks);
 
 }  // namespace ptoc

@@ -1,5 +1,8 @@
 // TREDUCE / reduce_scatter kernels for __half elements (one translation unit
 // per element type so the library builds in parallel).
+#include <atomic>
+
+#include "reduce_async.cuh"
 #include "reduce_impl.cuh"
 
 namespace ptoc {
@@ -10,5 +13,25 @@ cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, int unroll,
 }
 
 int occupancy_reduce_f16(int op, int vb, int unroll) { return occupancy_t<__half>(op, vb, unroll); }
+
+cudaError_t launch_async_f16(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s)
+{
+    return launch_async_t<__half>(p, op, cfg, grid, s);
+}
+
+// Resident CTAs per SM of the pipelined kernel on device `dev`, cached; the
+// first query of a device also opts the kernel into its shared-memory size.
+int occupancy_async_f16(int op, int cfg, int dev)
+{
+    static std::atomic<int> cache[kMaxDevices][3][kAsyncCfgs];
+    if (dev < 0 || dev >= kMaxDevices || op < 0 || op > 2 || cfg < 0 || cfg >= kAsyncCfgs)
+        return async_occupancy_t<__half>(op, cfg);
+    int v = cache[dev][op][cfg].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = async_occupancy_t<__half>(op, cfg);
+        cache[dev][op][cfg].store(v > 0 ? v : -1, std::memory_order_relaxed);
+    }
+    return v > 0 ? v : 0;
+}
 
 }  // namespace ptoc
