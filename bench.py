@@ -78,7 +78,7 @@ class TreduceBench(Workload):
     def __init__(self, w, storage):
         self.w, self.storage = w, storage
         self.name = w.name
-        self.kernel = "reduce_kernel (%s)" % storage
+        self.kernel = "reduce_async_kernel<%s> (shared-memory pipeline)" % storage
         self.dtype_compute = "i32" if storage == "i32" else "f32"
 
     def bytes_per_launch(self):
@@ -173,7 +173,7 @@ class RsAgBench(Workload):
         self.cfg = synth.CONFIG4
         self.name = "reduce_scatter_allgather_n8_f16_8192x4096"
         self.storage = "f16"
-        self.kernel = "reduce_kernel (f16, scatter) + gather_kernel"
+        self.kernel = "reduce_async_kernel<f16> (scatter mode) + gather_kernel"
 
     def bytes_per_launch_list(self):
         c = self.cfg
