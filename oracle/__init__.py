@@ -22,8 +22,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-# ReduceOp values (TREDUCE article, section 1.3).
-SUM, MAX, MIN = 0, 1, 2
+# ReduceOp values (TREDUCE article, section 1.3; Prod appended by the
+# Distributed Operators page's ABI enums).
+SUM, MAX, MIN, PROD = 0, 1, 2, 3
+# AtomicType values (Distributed Operators page, ABI enums).
+ATOMIC_NONE, ATOMIC_ADD = 0, 1
 # The oracle's element-type codes.
 F32, F16, BF16, I32 = 0, 1, 2, 3
 ELEM_BYTES = {F32: 4, F16: 2, BF16: 2, I32: 4}
@@ -62,8 +65,14 @@ def lib():
         L.oracle_all_to_all_v.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
                                           ctypes.POINTER(vp), ctypes.POINTER(vp),
                                           i32, i64, i64, i32]
+        L.oracle_allreduce.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
+        L.oracle_broadcast.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i64, i64, i32]
+        L.oracle_all_to_all.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i64, i64, i32]
+        L.oracle_all_to_all_v_combine.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                  ctypes.POINTER(vp), i32, i64, i64, i32, i32]
         for name in ("oracle_treduce", "oracle_reduce_scatter", "oracle_allgather",
-                     "oracle_all_to_all_v"):
+                     "oracle_all_to_all_v", "oracle_allreduce", "oracle_broadcast",
+                     "oracle_all_to_all", "oracle_all_to_all_v_combine"):
             getattr(L, name).restype = ctypes.c_int
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
@@ -109,6 +118,27 @@ def all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows, size, e
         assert c.dtype == np.int32
     return lib().oracle_all_to_all_v(_ptrs(inputs), _ptrs(targets), _ptrs(send_counts),
                                      _ptrs(recv_counts), n, target_rows, size, elem_size)
+
+
+def allreduce(windows, rows, cols, ld, op, dtype):
+    return lib().oracle_allreduce(_ptrs(windows), len(windows), rows, cols, ld, op, dtype)
+
+
+def broadcast(windows, root, rows, cols, ld, dtype):
+    return lib().oracle_broadcast(_ptrs(windows), len(windows), root, rows, cols, ld, dtype)
+
+
+def all_to_all(inputs, targets, target_rows, size, elem_size):
+    assert len(targets) == len(inputs)
+    return lib().oracle_all_to_all(_ptrs(inputs), _ptrs(targets), len(inputs), target_rows, size,
+                                   elem_size)
+
+
+def all_to_all_v_combine(windows, outputs, recv_counts, target_rows, size, atomic, dtype):
+    n = len(windows)
+    assert len(outputs) == n and len(recv_counts) == n
+    return lib().oracle_all_to_all_v_combine(_ptrs(windows), _ptrs(outputs), _ptrs(recv_counts), n,
+                                             target_rows, size, atomic, dtype)
 
 
 def f32_to_bf16(x):

@@ -27,8 +27,12 @@
 #include <string.h>
 #include <math.h>
 
-/* ReduceOp values: [TR] §1.3 (Sum = 0, Max = 1, Min = 2). */
-enum { ORC_SUM = 0, ORC_MAX = 1, ORC_MIN = 2 };
+/* ReduceOp values: [TR] §1.3 (Sum = 0, Max = 1, Min = 2); [DO] "ABI enums"
+ * appends kProd = 3 for the allreduce family. */
+enum { ORC_SUM = 0, ORC_MAX = 1, ORC_MIN = 2, ORC_PROD = 3 };
+/* AtomicType values ([DO] "ABI enums"): plain store, or add into the
+ * destination. */
+enum { ORC_ATOMIC_NONE = 0, ORC_ATOMIC_ADD = 1 };
 /* Element types the oracle accepts (its own numbering, passed by the tests). */
 enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_I32 = 3 };
 enum { ORC_OK = 0, ORC_BAD_ARG = 1 };
@@ -200,6 +204,7 @@ static void treduce_element(const void* const* src, const int* order, int nranks
         for (int t = 1; t < nranks; ++t) {
             int32_t x = ((const int32_t*)src[order[t]])[k];
             if (op == ORC_SUM) acc = (int32_t)((uint32_t)acc + (uint32_t)x);
+            else if (op == ORC_PROD) acc = (int32_t)((uint32_t)acc * (uint32_t)x);   /* wraps too */
             else if (op == ORC_MAX) acc = (x > acc) ? x : acc;
             else acc = (x < acc) ? x : acc;
         }
@@ -207,14 +212,17 @@ static void treduce_element(const void* const* src, const int* order, int nranks
         return;
     }
 
-    if (op == ORC_SUM) {
-        /* acc = W(root); acc = acc + W(src_r) for the rest in order; one RNE
-         * narrowing at the end. Accumulation in binary32 for every floating
-         * type (reading: the pages make the accumulator tile the destination
-         * type; the fp32 accumulator is the library's stated contract). */
+    if (op == ORC_SUM || op == ORC_PROD) {
+        /* acc = W(root); acc = acc + W(src_r) (or acc * W(src_r)) for the rest
+         * in order; one RNE narrowing at the end. Accumulation in binary32 for
+         * every floating type (reading: the pages make the accumulator tile the
+         * destination type; the fp32 accumulator is the library's stated
+         * contract). */
         float acc = widen(dtype, src[order[0]], k);
-        for (int t = 1; t < nranks; ++t)
-            acc = acc + widen(dtype, src[order[t]], k);
+        for (int t = 1; t < nranks; ++t) {
+            if (op == ORC_SUM) acc = acc + widen(dtype, src[order[t]], k);
+            else acc = acc * widen(dtype, src[order[t]], k);
+        }
         narrow_store(dtype, dst, k, acc);
         return;
     }
@@ -247,7 +255,7 @@ int oracle_treduce(const void* const* src, int nranks, int root, void* dst,
                    int64_t valid_rows, int64_t valid_cols, int64_t ld, int op, int dtype)
 {
     if (nranks <= 0 || root < 0 || root >= nranks) return ORC_BAD_ARG;   /* [TR] §3.3 */
-    if (op != ORC_SUM && op != ORC_MAX && op != ORC_MIN) return ORC_BAD_ARG;
+    if (op != ORC_SUM && op != ORC_MAX && op != ORC_MIN && op != ORC_PROD) return ORC_BAD_ARG;
     if (elem_bytes(dtype) == 0) return ORC_BAD_ARG;
     if (valid_rows < 0 || valid_cols < 0 || (valid_cols > ld && valid_rows > 0)) return ORC_BAD_ARG;
     if (valid_rows == 0 || valid_cols == 0) return ORC_OK;
@@ -283,7 +291,7 @@ int oracle_reduce_scatter(void* const* win, int nranks, int64_t rows, int64_t co
 {
     if (nranks <= 0 || rows < 0 || cols < 0 || (cols > ld && rows > 0)) return ORC_BAD_ARG;
     size_t b = elem_bytes(dtype);
-    if (b == 0 || (op != ORC_SUM && op != ORC_MAX && op != ORC_MIN)) return ORC_BAD_ARG;
+    if (b == 0 || (op != ORC_SUM && op != ORC_MAX && op != ORC_MIN && op != ORC_PROD)) return ORC_BAD_ARG;
     if (rows == 0 || cols == 0) return ORC_OK;
 
     size_t footprint = (size_t)((rows - 1) * ld + cols) * b;
@@ -361,6 +369,127 @@ int oracle_all_to_all_v(const void* const* inputs, void* const* targets,
                 memcpy((char*)targets[d] + (size_t)(s * max_recv + i) * row_bytes,
                        (const char*)inputs[s] + (size_t)(d * max_recv + i) * row_bytes,
                        row_bytes);
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* allreduce, broadcast, symmetric all_to_all                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * allreduce ([DO] "pld.tensor.allreduce": every participating rank's window
+ * slice is reduced in place; Sum, Max, Min and Prod). Reading: every window's
+ * [rows, cols] box becomes the same value, the reduction over all windows in
+ * rank order 0..N-1 (what reduce_scatter followed by allgather produces), so
+ * the ranks agree bit for bit. Computed from a snapshot taken before any write.
+ */
+int oracle_allreduce(void* const* win, int nranks, int64_t rows, int64_t cols,
+                     int64_t ld, int op, int dtype)
+{
+    if (nranks <= 0 || rows < 0 || cols < 0 || (cols > ld && rows > 0)) return ORC_BAD_ARG;
+    size_t b = elem_bytes(dtype);
+    if (b == 0 || (op != ORC_SUM && op != ORC_MAX && op != ORC_MIN && op != ORC_PROD)) return ORC_BAD_ARG;
+    if (rows == 0 || cols == 0) return ORC_OK;
+    size_t footprint = (size_t)((rows - 1) * ld + cols) * b;
+    void** snap = (void**)malloc(sizeof(void*) * (size_t)nranks);
+    for (int r = 0; r < nranks; ++r) {
+        snap[r] = malloc(footprint);
+        memcpy(snap[r], win[r], footprint);
+    }
+    for (int r = 0; r < nranks; ++r)
+        oracle_treduce((const void* const*)snap, nranks, 0, win[r], rows, cols, ld, op, dtype);
+    for (int r = 0; r < nranks; ++r) free(snap[r]);
+    free(snap);
+    return ORC_OK;
+}
+
+/*
+ * broadcast ([DO] op table: "replicate root rank's data to all ranks", the
+ * result is the window): every other window's [rows, cols] box becomes the
+ * root's, bit for bit.
+ */
+int oracle_broadcast(void* const* win, int nranks, int root, int64_t rows, int64_t cols,
+                     int64_t ld, int dtype)
+{
+    if (nranks <= 0 || root < 0 || root >= nranks || rows < 0 || cols < 0 || (cols > ld && rows > 0))
+        return ORC_BAD_ARG;
+    size_t b = elem_bytes(dtype);
+    if (b == 0) return ORC_BAD_ARG;
+    for (int s = 0; s < nranks; ++s) {
+        if (s == root) continue;
+        for (int64_t i = 0; i < rows; ++i)
+            memcpy((char*)win[s] + (size_t)(i * ld) * b, (const char*)win[root] + (size_t)(i * ld) * b,
+                   (size_t)cols * b);
+    }
+    return ORC_OK;
+}
+
+/*
+ * symmetric all_to_all ([DO] op table: every rank pushes its per-destination
+ * chunks to every peer's window). With C = target_rows / N rows per chunk:
+ *   target_d rows [s*C, (s+1)*C) = input_s rows [d*C, (d+1)*C)
+ * for every (s, d), s == d included; rows at and past N*C are not written.
+ */
+int oracle_all_to_all(const void* const* inputs, void* const* targets, int nranks,
+                      int64_t target_rows, int64_t size, int elem_size)
+{
+    if (nranks <= 0 || target_rows < 0 || size < 0 || elem_size <= 0) return ORC_BAD_ARG;
+    int64_t chunk = target_rows / nranks;
+    size_t row_bytes = (size_t)size * (size_t)elem_size;
+    for (int s = 0; s < nranks; ++s)
+        for (int d = 0; d < nranks; ++d)
+            for (int64_t i = 0; i < chunk; ++i)
+                memcpy((char*)targets[d] + (size_t)(s * chunk + i) * row_bytes,
+                       (const char*)inputs[s] + (size_t)(d * chunk + i) * row_bytes, row_bytes);
+    return ORC_OK;
+}
+
+/*
+ * all_to_all_v combine: the return leg of all_to_all_v, a put from every
+ * rank d to every peer s ([DO] "pld.tensor.put" and "pld.tile.remote_store":
+ * atomic = kAdd makes the push a combine, peer_region += src, "what an
+ * all-to-all combine needs"). With MAX_RECV = target_rows / N and
+ * c = clamp(recv_counts_d[s], 0, MAX_RECV), the c rows rank d received from s
+ * (its window rows [s*MAX_RECV, s*MAX_RECV + c)) go back to rank s's output
+ * rows [d*MAX_RECV, d*MAX_RECV + c):
+ *   kNone: output_s row = window_d row, bit for bit;
+ *   kAdd:  output_s element = N(W(output_s element) + W(window_d element))
+ *          (binary32 add, one RNE narrowing; int32 wraps).
+ * Every output row has at most one contributor, so the result does not depend
+ * on the order of the pushes. Rows outside the counts are not written.
+ */
+int oracle_all_to_all_v_combine(const void* const* windows, void* const* outputs,
+                                const int32_t* const* recv_counts, int nranks,
+                                int64_t target_rows, int64_t size, int atomic, int dtype)
+{
+    if (nranks <= 0 || target_rows < 0 || size < 0) return ORC_BAD_ARG;
+    size_t b = elem_bytes(dtype);
+    if (b == 0 || (atomic != ORC_ATOMIC_NONE && atomic != ORC_ATOMIC_ADD)) return ORC_BAD_ARG;
+    int64_t max_recv = target_rows / nranks;
+    for (int d = 0; d < nranks; ++d) {
+        for (int s = 0; s < nranks; ++s) {
+            int64_t c = recv_counts[d][s];
+            if (c < 0) c = 0;
+            if (c > max_recv) c = max_recv;
+            for (int64_t i = 0; i < c; ++i) {
+                const char* src = (const char*)windows[d] + (size_t)((s * max_recv + i) * size) * b;
+                char* dst = (char*)outputs[s] + (size_t)((d * max_recv + i) * size) * b;
+                if (atomic == ORC_ATOMIC_NONE) {
+                    memcpy(dst, src, (size_t)size * b);
+                    continue;
+                }
+                for (int64_t j = 0; j < size; ++j) {
+                    if (dtype == ORC_I32) {
+                        ((int32_t*)dst)[j] = (int32_t)((uint32_t)((int32_t*)dst)[j] +
+                                                       (uint32_t)((const int32_t*)src)[j]);
+                    } else {
+                        float acc = widen(dtype, dst, j) + widen(dtype, src, j);
+                        narrow_store(dtype, dst, j, acc);
+                    }
+                }
+            }
         }
     }
     return ORC_OK;
