@@ -10,7 +10,7 @@
  *        lpnh.cn news 2291107), sections 1-8.
  *   [DO] "Distributed Operators (N6)" (pypto.ai dev/distributed_ops): the op
  *        table in "Overview", "ABI enums", "pld.tensor.all_to_all_v",
- *        "pld.tensor.allreduce".
+ *        "pld.tensor.allreduce", "pld.tensor.put", "pld.tile.remote_store".
  *
  * Conventions shared by every entry point
  *   - Every data pointer is a DEVICE pointer on the calling thread's current
@@ -58,8 +58,10 @@ typedef enum {
 } ptoc_status;
 
 /* Reduction operators. Values follow the ReduceOp ABI ([TR] §1.3: Sum = 0,
- * Max = 1, Min = 2; [DO] "ABI enums" appends kProd = 3, which this library
- * reserves: PTOC_PROD returns PTOC_ERR_UNSUPPORTED). */
+ * Max = 1, Min = 2; [DO] "ABI enums" appends kProd = 3 for the allreduce
+ * family). TREDUCE takes Sum, Max and Min only (PTOC_PROD returns
+ * PTOC_ERR_UNSUPPORTED there); reduce_scatter and allreduce take all four.
+ * Prod multiplies in binary32 one rank at a time (int32 wraps modulo 2^32). */
 typedef enum {
     PTOC_SUM = 0,
     PTOC_MAX = 1,
@@ -74,6 +76,13 @@ typedef enum {
     PTOC_BF16 = 2,
     PTOC_I32 = 3
 } ptoc_dtype;
+
+/* Store semantics of a put ([DO] "ABI enums", AtomicType): overwrite the
+ * destination, or add into it (a combine, dst += src). */
+typedef enum {
+    PTOC_ATOMIC_NONE = 0,
+    PTOC_ATOMIC_ADD = 1
+} ptoc_atomic_type;
 
 /* A rank group ([TR] §2.1, §3.3, §6: ParallelGroup{tensors, nranks, rootIdx}).
  * tensors: host array of nranks device pointers, tensors[r] = rank r's slice.
@@ -116,8 +125,8 @@ ptoc_status ptoc_treduce(const ptoc_group* group, void* dst,
  * segment bounds of [DO] "pld.tensor.allreduce", ring mode, applied to rows)
  * becomes the reduction over all windows of the same rows, columns
  * [0, cols), in rank order 0..N-1, binary32 accumulation. Every other element
- * of every window is left unchanged. windows->root is ignored.
- * Windows must not overlap one another (PTOC_ERR_ALIAS).
+ * of every window is left unchanged. windows->root is ignored. op: Sum, Max,
+ * Min or Prod. Windows must not overlap one another (PTOC_ERR_ALIAS).
  */
 ptoc_status ptoc_reduce_scatter(const ptoc_group* windows,
                                 int64_t rows, int64_t cols, int64_t ld,
@@ -132,6 +141,32 @@ ptoc_status ptoc_reduce_scatter(const ptoc_group* windows,
  * windows->root is ignored. Windows must not overlap (PTOC_ERR_ALIAS).
  */
 ptoc_status ptoc_allgather(const ptoc_group* windows,
+                           int64_t rows, int64_t cols, int64_t ld,
+                           ptoc_dtype dtype, cudaStream_t stream);
+
+/*
+ * ptoc_allreduce - allreduce over N windows, in place ([DO]
+ * "pld.tensor.allreduce": every participating rank's window slice is reduced
+ * in place; Sum, Max, Min, Prod). Every window's [rows, cols] box becomes the
+ * same value: the reduction over all windows in rank order 0..N-1 with binary32
+ * accumulation, bit-identical to ptoc_reduce_scatter followed by
+ * ptoc_allgather with the same arguments, done in one pass (each element is
+ * read once from every window and written once to every window). Columns
+ * [cols, ld) are untouched. windows->root is ignored. Windows must not overlap
+ * (PTOC_ERR_ALIAS).
+ */
+ptoc_status ptoc_allreduce(const ptoc_group* windows,
+                           int64_t rows, int64_t cols, int64_t ld,
+                           ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream);
+
+/*
+ * ptoc_broadcast - broadcast into N windows, in place ([DO] op table:
+ * "replicate root rank's data to all ranks"; the result is the window). The
+ * [rows, cols] box of window windows->root is copied bit for bit into every
+ * other window. Requires root in [0, N). Windows must not overlap
+ * (PTOC_ERR_ALIAS).
+ */
+ptoc_status ptoc_broadcast(const ptoc_group* windows,
                            int64_t rows, int64_t cols, int64_t ld,
                            ptoc_dtype dtype, cudaStream_t stream);
 
@@ -162,6 +197,43 @@ ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* target
                               const int32_t* const* send_counts, int32_t* const* recv_counts,
                               int64_t target_rows, int64_t size, ptoc_dtype dtype,
                               cudaStream_t stream);
+
+/*
+ * ptoc_all_to_all - symmetric all-to-all ([DO] op table: every rank pushes
+ * its per-destination chunks to every peer's window; the window is the
+ * result). Layout as ptoc_all_to_all_v with C = target_rows / N rows per
+ * chunk: targets[d] rows [s*C, (s+1)*C) = inputs[s] rows [d*C, (d+1)*C) for
+ * every (s, d). Rows at and past N*C are not written. Alias rules as
+ * ptoc_all_to_all_v (targets must not overlap inputs or each other).
+ */
+ptoc_status ptoc_all_to_all(const ptoc_group* inputs, const ptoc_group* targets,
+                            int64_t target_rows, int64_t size, ptoc_dtype dtype,
+                            cudaStream_t stream);
+
+/*
+ * ptoc_all_to_all_v_combine - the return leg of ptoc_all_to_all_v: a put from
+ * every rank d to every peer s ([DO] "pld.tensor.put", "pld.tile.remote_store":
+ * AtomicType kAdd makes the push a combine, peer_region += src, what an
+ * all-to-all combine needs).
+ *   windows->tensors[d] : rank d's window [target_rows, size] holding the rows
+ *                         it received (read)
+ *   outputs->tensors[s] : rank s's output [target_rows, size] (written)
+ *   recv_counts[d]      : host array of N device pointers, each int32[N]: the
+ *                         rows rank d holds from each source (read; typically
+ *                         the counts ptoc_all_to_all_v published)
+ * With MAX_RECV = target_rows / N and c = clamp(recv_counts[d][s], 0,
+ * MAX_RECV): outputs[s] rows [d*MAX_RECV, d*MAX_RECV + c) receive windows[d]
+ * rows [s*MAX_RECV, s*MAX_RECV + c); PTOC_ATOMIC_NONE overwrites bit for bit,
+ * PTOC_ATOMIC_ADD adds (binary32 add and one RNE narrowing per element for
+ * floating types, wrapping for int32). Every output row has at most one
+ * contributor, so the result does not depend on scheduling. Other output rows
+ * are not written. Outputs must not overlap each other, the windows or the
+ * counts (PTOC_ERR_ALIAS).
+ */
+ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, const ptoc_group* outputs,
+                                      const int32_t* const* recv_counts,
+                                      int64_t target_rows, int64_t size, ptoc_atomic_type atomic,
+                                      ptoc_dtype dtype, cudaStream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char* ptoc_status_string(ptoc_status status);

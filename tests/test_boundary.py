@@ -23,8 +23,9 @@ def declared_functions():
 
 
 def test_header_declares_the_abi():
-    assert declared_functions() == ["ptoc_all_to_all_v", "ptoc_allgather", "ptoc_reduce_scatter",
-                                    "ptoc_status_string", "ptoc_treduce"]
+    assert declared_functions() == ["ptoc_all_to_all", "ptoc_all_to_all_v", "ptoc_all_to_all_v_combine",
+                                    "ptoc_allgather", "ptoc_allreduce", "ptoc_broadcast",
+                                    "ptoc_reduce_scatter", "ptoc_status_string", "ptoc_treduce"]
 
 
 def test_library_exports_every_declared_symbol():
@@ -93,7 +94,7 @@ def test_reduce_scatter_and_allgather_reject():
     w = srcs(4)
     overl = [A, A + 100, A + 2 * 64 * MB, A + 3 * 64 * MB]
     assert P.ptoc_reduce_scatter(overl, 64, 64, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_ALIAS
-    assert P.ptoc_reduce_scatter(w, 64, 64, 64, P.PROD, P.F32, stream=0, check=False) == P.ERR_UNSUPPORTED
+    assert P.ptoc_reduce_scatter(w, 64, 64, 64, 7, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
     assert P.ptoc_reduce_scatter(w, 64, 65, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
     assert P.ptoc_reduce_scatter(w, 64, 64, 64, P.SUM, 5, stream=0, check=False) == P.ERR_INVALID_ARG
     assert P.ptoc_reduce_scatter([], 64, 64, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
@@ -126,3 +127,37 @@ def test_all_to_all_v_rejects():
     assert a2av(targets=[A + 8 * 64 * MB, A + 8 * 64 * MB + 64] + srcs(2, base=A + 10 * 64 * MB)) == P.ERR_ALIAS
     assert a2av(rc=[A + 16 * 64 * MB + 4] + [A + 17 * 64 * MB + 256 * r for r in range(1, 4)]) == P.ERR_ALIAS
     assert a2av(rc=[A + 8 * 64 * MB + 8] + [A + 17 * 64 * MB + 256 * r for r in range(1, 4)]) == P.ERR_ALIAS
+
+
+def test_allreduce_and_broadcast_reject():
+    w = srcs(4)
+    overl = [A, A + 100, A + 2 * 64 * MB, A + 3 * 64 * MB]
+    assert P.ptoc_allreduce(overl, 64, 64, 64, P.SUM, P.F32, stream=0, check=False) == P.ERR_ALIAS
+    assert P.ptoc_allreduce(w, 64, 64, 64, 7, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_allreduce(w, 64, 65, 64, P.PROD, P.F32, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_allreduce(w, 0, 64, 64, P.PROD, P.F32, stream=0, check=False) == P.OK
+    assert P.ptoc_allreduce([A], 64, 64, 64, P.PROD, P.F32, stream=0, check=False) == P.OK    # one rank
+    assert P.ptoc_reduce_scatter(w, 0, 64, 64, P.PROD, P.F32, stream=0, check=False) == P.OK  # Prod allowed
+    assert P.ptoc_broadcast(w, 64, 64, 64, P.F32, stream=0, root=4, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_broadcast(w, 64, 64, 64, P.F32, stream=0, root=-1, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_broadcast(overl, 64, 64, 64, P.F32, stream=0, root=0, check=False) == P.ERR_ALIAS
+    assert P.ptoc_broadcast(w, 64, 0, 64, P.F32, stream=0, root=1, check=False) == P.OK
+
+
+def test_all_to_all_and_combine_reject():
+    ins, tgs = srcs(4), srcs(4, base=A + 8 * 64 * MB)
+    assert P.ptoc_all_to_all(ins, tgs[:3], 64, 16, P.BF16, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_all_to_all(ins, [A] + tgs[1:], 64, 16, P.BF16, stream=0, check=False) == P.ERR_ALIAS
+    assert P.ptoc_all_to_all(ins, tgs, -1, 16, P.BF16, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_all_to_all(ins, tgs, 3, 16, P.BF16, stream=0, check=False) == P.OK      # chunk 0
+    rc = [A + 17 * 64 * MB + 256 * r for r in range(4)]
+    C = P.ptoc_all_to_all_v_combine
+    assert C(ins, tgs, rc, 64, 16, 2, P.BF16, stream=0, check=False) == P.ERR_INVALID_ARG  # atomic
+    assert C(ins, tgs, rc, 64, 16, P.ATOMIC_ADD, 9, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert C(ins, [A + 64 * MB] + tgs[1:], rc, 64, 16, P.ATOMIC_ADD, P.BF16, stream=0,
+             check=False) == P.ERR_ALIAS                                                   # output = window
+    assert C(ins, [rc[0] - 8] + tgs[1:], rc, 64, 16, P.ATOMIC_ADD, P.BF16, stream=0,
+             check=False) == P.ERR_ALIAS                                                   # output over counts
+    assert C(ins, tgs, [rc[0] + 2] + rc[1:], 64, 16, P.ATOMIC_NONE, P.BF16, stream=0,
+             check=False) == P.ERR_INVALID_ARG                                             # misaligned counts
+    assert C(ins, tgs, rc, 3, 16, P.ATOMIC_ADD, P.BF16, stream=0, check=False) == P.OK     # MAX_RECV 0

@@ -13,6 +13,11 @@ Entry points carry the C names:
     ptoc_allgather(windows, rows, cols, ld, dtype, stream=None)
     ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows,
                       size, dtype, stream=None)
+    ptoc_allreduce(windows, rows, cols, ld, op, dtype, stream=None)
+    ptoc_broadcast(windows, rows, cols, ld, dtype, stream=None, root=0)
+    ptoc_all_to_all(inputs, targets, target_rows, size, dtype, stream=None)
+    ptoc_all_to_all_v_combine(windows, outputs, recv_counts, target_rows, size,
+                              atomic, dtype, stream=None)
 
 Buffers are torch tensors or raw device addresses (ints). ``stream=None``
 means torch's current stream. A non-OK status raises :class:`PtocError`
@@ -40,6 +45,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA = 0, 1, 2, 3, 4
 SUM, MAX, MIN, PROD = 0, 1, 2, 3
 F32, F16, BF16, I32 = 0, 1, 2, 3
+ATOMIC_NONE, ATOMIC_ADD = 0, 1
 MAX_RANKS = 64
 
 OPS = {"sum": SUM, "max": MAX, "min": MIN, "prod": PROD}
@@ -58,7 +64,13 @@ _lib.ptoc_reduce_scatter.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, ctypes.
 _lib.ptoc_allgather.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, _vp]
 _lib.ptoc_all_to_all_v.argtypes = [_G, _G, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i64, _i64,
                                    ctypes.c_int, _vp]
-for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v"):
+_lib.ptoc_allreduce.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]
+_lib.ptoc_broadcast.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, _vp]
+_lib.ptoc_all_to_all.argtypes = [_G, _G, _i64, _i64, ctypes.c_int, _vp]
+_lib.ptoc_all_to_all_v_combine.argtypes = [_G, _G, ctypes.POINTER(_vp), _i64, _i64, ctypes.c_int,
+                                           ctypes.c_int, _vp]
+for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v",
+           "ptoc_allreduce", "ptoc_broadcast", "ptoc_all_to_all", "ptoc_all_to_all_v_combine"):
     getattr(_lib, _f).restype = ctypes.c_int
 _lib.ptoc_status_string.argtypes = [ctypes.c_int]
 _lib.ptoc_status_string.restype = ctypes.c_char_p
@@ -140,6 +152,36 @@ def ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows, si
     return _done(st, "ptoc_all_to_all_v", check)
 
 
+def ptoc_allreduce(windows, rows, cols, ld, op, dtype, stream=None, check=True):
+    g, keep = _group(windows)
+    st = _lib.ptoc_allreduce(ctypes.byref(g), rows, cols, ld, int(op), int(dtype), _stream(stream))
+    return _done(st, "ptoc_allreduce", check)
+
+
+def ptoc_broadcast(windows, rows, cols, ld, dtype, stream=None, root=0, check=True):
+    g, keep = _group(windows, root)
+    st = _lib.ptoc_broadcast(ctypes.byref(g), rows, cols, ld, int(dtype), _stream(stream))
+    return _done(st, "ptoc_broadcast", check)
+
+
+def ptoc_all_to_all(inputs, targets, target_rows, size, dtype, stream=None, check=True):
+    gi, k1 = _group(inputs)
+    gt, k2 = _group(targets)
+    st = _lib.ptoc_all_to_all(ctypes.byref(gi), ctypes.byref(gt), target_rows, size, int(dtype),
+                              _stream(stream))
+    return _done(st, "ptoc_all_to_all", check)
+
+
+def ptoc_all_to_all_v_combine(windows, outputs, recv_counts, target_rows, size, atomic, dtype,
+                              stream=None, check=True):
+    gw, k1 = _group(windows)
+    go, k2 = _group(outputs)
+    rc = _ptr_array(recv_counts)
+    st = _lib.ptoc_all_to_all_v_combine(ctypes.byref(gw), ctypes.byref(go), rc, target_rows, size,
+                                        int(atomic), int(dtype), _stream(stream))
+    return _done(st, "ptoc_all_to_all_v_combine", check)
+
+
 # ---- shape-inferring conveniences over torch tensors ------------------------
 
 def dtype_code(t):
@@ -182,3 +224,26 @@ def all_to_all_v(inputs, targets, send_counts, recv_counts, stream=None):
     tr, size = targets[0].shape
     return ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, tr, size,
                              dtype_code(targets[0]), stream=stream)
+
+
+def allreduce(windows, op="sum", stream=None):
+    rows, cols, ld = _rows_cols_ld(windows[0])
+    return ptoc_allreduce(windows, rows, cols, ld, OPS[op] if isinstance(op, str) else op,
+                          dtype_code(windows[0]), stream=stream)
+
+
+def broadcast(windows, root=0, stream=None):
+    rows, cols, ld = _rows_cols_ld(windows[0])
+    return ptoc_broadcast(windows, rows, cols, ld, dtype_code(windows[0]), stream=stream, root=root)
+
+
+def all_to_all(inputs, targets, stream=None):
+    tr, size = targets[0].shape
+    return ptoc_all_to_all(inputs, targets, tr, size, dtype_code(targets[0]), stream=stream)
+
+
+def all_to_all_v_combine(windows, outputs, recv_counts, atomic="none", stream=None):
+    tr, size = outputs[0].shape
+    a = {"none": ATOMIC_NONE, "add": ATOMIC_ADD}[atomic] if isinstance(atomic, str) else atomic
+    return ptoc_all_to_all_v_combine(windows, outputs, recv_counts, tr, size, a,
+                                     dtype_code(outputs[0]), stream=stream)

@@ -1,18 +1,24 @@
-// Window-layout data movement: allgather and all_to_all_v.
+// Window-layout data movement ("Distributed Operators (N6)"): allgather,
+// broadcast, all_to_all_v, symmetric all_to_all and the all_to_all_v combine.
 //
-// allgather ("Distributed Operators (N6)", op table): row chunk r of window r
-// is copied into row chunk r of every other window. One read, N-1 writes per
-// element: each thread loads its vectors once and stores them N-1 times.
+// allgather (op table): row chunk r of window r is copied into row chunk r of
+// every other window. broadcast (op table): the root's rows are copied into
+// every other window. One read, N-1 writes per element: each thread loads its
+// vectors once and stores them N-1 times.
 //
-// all_to_all_v ("Distributed Operators (N6)", pld.tensor.all_to_all_v): for
-// every (sender s, destination d) the clamped count c = clamp(send_counts[s][d],
-// 0, MAX_RECV) is published to recv_counts[d][s], and c packed rows move from
-// input s (rows d*MAX_RECV ..) to target d (rows s*MAX_RECV ..). Because the
-// rows of one pair are contiguous on both sides, each pair is one contiguous
-// copy of c * row_bytes bytes. The counts live on the device, so the grid
-// cannot be sized from them: a persistent grid walks a list of fixed-size
-// tiles, and every CTA rebuilds the per-pair tile prefix sums in shared memory
-// from the N^2 counts (a few hundred integers, L2-resident) before it starts.
+// all_to_all_v (pld.tensor.all_to_all_v): for every (sender s, destination
+// d) the clamped count c = clamp(send_counts[s][d], 0, MAX_RECV) is published
+// to recv_counts[d][s], and c packed rows move from input s (rows
+// d*MAX_RECV ..) to target d (rows s*MAX_RECV ..). The symmetric all_to_all
+// (op table) is the same exchange with every count equal to MAX_RECV. The
+// combine (pld.tensor.put / remote_store with AtomicType kAdd) is the return
+// leg: rank d pushes the recv_counts[d][s] rows it holds from s back to s's
+// output, overwriting or adding. Because the rows of one pair are contiguous
+// on both sides, each pair is one contiguous copy of c * row_bytes bytes. The
+// counts live on the device, so the grid cannot be sized from them: a
+// persistent grid walks a list of fixed-size tiles, and every CTA rebuilds the
+// per-pair tile prefix sums in shared memory from the N^2 counts (a few
+// hundred integers, L2-resident) before it starts.
 #include <cuda_runtime.h>
 
 #include "ptoc_internal.h"
@@ -44,7 +50,7 @@ __global__ void __launch_bounds__(kBlock) gather_kernel(const __grid_constant__ 
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const int64_t row = t / p.tpr;
         const int64_t seg = t - row * p.tpr;
-        const int owner = row_owner(row, n, p.rows);
+        const int owner = p.root >= 0 ? p.root : row_owner(row, n, p.rows);
         const int64_t row_byte = row * p.ld * EB;
         const int64_t v = seg * kBlock + threadIdx.x;
         if (v < p.vpr) {
@@ -93,10 +99,10 @@ __device__ __forceinline__ int32_t clamp_count(int32_t c, int64_t max_recv)
 }
 
 // Per-pair state in shared memory: cnt[q] = clamped count of pair q
-// (q = s * N + d), pre[q] = tiles of pairs 0..q-1 (exclusive prefix), pre[np]
+// (q = a * N + b), pre[q] = tiles of pairs 0..q-1 (exclusive prefix), pre[np]
 // = total. Each thread scans a contiguous run of pairs; the run totals are
 // combined with a warp-shuffle scan and a pass over the warp totals. Block 0
-// also publishes the counts to recv_counts.
+// also publishes the counts when asked (all_to_all_v's recv_counts).
 __device__ void build_pairs(const A2avParams& p, int32_t* cnt, int32_t* pre, int32_t* warp_tot)
 {
     const int n = p.nranks;
@@ -107,9 +113,9 @@ __device__ void build_pairs(const A2avParams& p, int32_t* cnt, int32_t* pre, int
 
     int32_t run = 0;
     for (int q = q0; q < q1; ++q) {
-        const int s = q / n, d = q - (q / n) * n;
-        const int32_t c = clamp_count(p.sc[s][d], p.max_recv);
-        if (blockIdx.x == 0) p.rc[d][s] = c;
+        const int a = q / n, b = q - (q / n) * n;
+        const int32_t c = p.full ? (int32_t)p.max_recv : clamp_count(p.cnt[a][b], p.max_recv);
+        if (p.publish && blockIdx.x == 0) p.pub[b][a] = c;
         cnt[q] = c;
         const int32_t tiles = (int32_t)(((int64_t)c * p.row_bytes + p.tile_bytes - 1) / p.tile_bytes);
         pre[q] = tiles;                 // temporarily: this pair's tile count
@@ -144,13 +150,51 @@ __device__ void build_pairs(const A2avParams& p, int32_t* cnt, int32_t* pre, int
     __syncthreads();
 }
 
+// Moves one chunk of VB bytes: a copy, or (AddMover) out += in per element.
+template <int VB>
+struct CopyMover {
+    using C = Chunk<VB>;
+    using V = typename C::type;
+    static __device__ __forceinline__ V load(const char* src, const char*) { return C::load(src); }
+    static __device__ __forceinline__ void store(char* dst, const V& v) { C::store(dst, v); }
+};
+
+template <class T, int VB>
+struct AddMover {
+    static constexpr int W = VB / 4;
+    using V = Words<W>;
+    // loads both operands and returns the sum, ready to store
+    static __device__ __forceinline__ V load(const char* src, const char* dst)
+    {
+        VecAcc<T, kSum, W> acc;
+        acc.init(load_words<W>(dst));
+        acc.add(load_words<W>(src));
+        return acc.out();
+    }
+    static __device__ __forceinline__ void store(char* dst, const V& v) { store_words<W>(dst, v); }
+};
+
+// 16-bit data that is only 2-byte aligned: one element at a time.
+template <class T>
+struct AddMover1 {
+    using V = Elem16;
+    static __device__ __forceinline__ V load(const char* src, const char* dst)
+    {
+        const float a = Scalar<T>::widen(Chunk<2>::load(dst).h);
+        const float b = Scalar<T>::widen(Chunk<2>::load(src).h);
+        V r;
+        r.h = Scalar<T>::narrow(__fadd_rn(a, b));
+        return r;
+    }
+    static __device__ __forceinline__ void store(char* dst, const V& v) { Chunk<2>::store(dst, v); }
+};
+
 // U chunks of VB bytes per thread per tile: tile_bytes = U * kBlock * VB.
-template <int VB, int U>
-__global__ void __launch_bounds__(kBlock) a2av_kernel(const __grid_constant__ A2avParams p)
+template <class M, int VB, int U>
+__global__ void __launch_bounds__(kBlock) pairs_kernel(const __grid_constant__ A2avParams p)
 {
     extern __shared__ int32_t smem[];
     __shared__ int32_t warp_tot[kBlock / 32];
-    using C = Chunk<VB>;
     const int n = p.nranks;
     const int np = n * n;
     int32_t* cnt = smem;                    // np entries
@@ -167,23 +211,23 @@ __global__ void __launch_bounds__(kBlock) a2av_kernel(const __grid_constant__ A2
             else hi = mid;
         }
         const int q = lo;
-        const int s = q / n, d = q - (q / n) * n;
+        const int a = q / n, b = q - (q / n) * n;
         const int64_t bytes = (int64_t)cnt[q] * p.row_bytes;
         const int64_t beg = (int64_t)(t - pre[q]) * p.tile_bytes;
         const int64_t len = min(p.tile_bytes, bytes - beg);
-        const char* src = (const char*)p.in[s] + d * p.max_recv * p.row_bytes + beg;
-        char* dst = (char*)p.tgt[d] + s * p.max_recv * p.row_bytes + beg;
+        const char* src = (const char*)p.in[a] + b * p.max_recv * p.row_bytes + beg;
+        char* dst = (char*)p.out[b] + a * p.max_recv * p.row_bytes + beg;
 
-        typename C::type x[U];
+        typename M::V x[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t o = ((int64_t)k * kBlock + threadIdx.x) * VB;
-            if (o < len) x[k] = C::load(src + o);
+            if (o < len) x[k] = M::load(src + o, dst + o);
         }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t o = ((int64_t)k * kBlock + threadIdx.x) * VB;
-            if (o < len) C::store(dst + o, x[k]);
+            if (o < len) M::store(dst + o, x[k]);
         }
     }
 }
@@ -194,10 +238,10 @@ template <int U>
 static cudaError_t launch_a2av_u(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
     const size_t smem = a2av_smem_bytes(p.nranks);
-    if (vb == 16) a2av_kernel<16, U><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 8) a2av_kernel<8, U><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 4) a2av_kernel<4, U><<<grid, kBlock, smem, s>>>(p);
-    else a2av_kernel<2, U><<<grid, kBlock, smem, s>>>(p);
+    if (vb == 16) pairs_kernel<CopyMover<16>, 16, U><<<grid, kBlock, smem, s>>>(p);
+    else if (vb == 8) pairs_kernel<CopyMover<8>, 8, U><<<grid, kBlock, smem, s>>>(p);
+    else if (vb == 4) pairs_kernel<CopyMover<4>, 4, U><<<grid, kBlock, smem, s>>>(p);
+    else pairs_kernel<CopyMover<2>, 2, U><<<grid, kBlock, smem, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -206,21 +250,74 @@ cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cuda
     return unroll == 8 ? launch_a2av_u<8>(p, vb, grid, s) : launch_a2av_u<4>(p, vb, grid, s);
 }
 
+template <class K>
+static int occupancy_of_kernel(K kernel, size_t smem)
+{
+    int b = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kBlock, smem);
+    return (e == cudaSuccess && b > 0) ? b : 1;
+}
+
 template <int U>
 static int a2av_occupancy_u(int vb, size_t smem)
 {
-    int b = 0;
-    cudaError_t e = vb == 16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<16, U>, kBlock, smem)
-                  : vb == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<8, U>, kBlock, smem)
-                  : vb == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<4, U>, kBlock, smem)
-                            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, a2av_kernel<2, U>, kBlock, smem);
-    return (e == cudaSuccess && b > 0) ? b : 1;
+    return vb == 16 ? occupancy_of_kernel(pairs_kernel<CopyMover<16>, 16, U>, smem)
+         : vb == 8 ? occupancy_of_kernel(pairs_kernel<CopyMover<8>, 8, U>, smem)
+         : vb == 4 ? occupancy_of_kernel(pairs_kernel<CopyMover<4>, 4, U>, smem)
+                   : occupancy_of_kernel(pairs_kernel<CopyMover<2>, 2, U>, smem);
 }
 
 int a2av_blocks_per_sm(int vb, int unroll, int nranks)
 {
     const size_t smem = a2av_smem_bytes(nranks);
     return unroll == 8 ? a2av_occupancy_u<8>(vb, smem) : a2av_occupancy_u<4>(vb, smem);
+}
+
+// The combine with kAdd: 4 chunks per thread per tile (each chunk loads both
+// operands).
+constexpr int kAddUnroll = 4;
+
+template <class T>
+static cudaError_t launch_add_t(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
+{
+    const size_t smem = a2av_smem_bytes(p.nranks);
+    if (vb == 16) pairs_kernel<AddMover<T, 16>, 16, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
+    else if (vb == 8) pairs_kernel<AddMover<T, 8>, 8, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
+    else if (vb == 4) pairs_kernel<AddMover<T, 4>, 4, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
+    else if constexpr (sizeof(T) == 2) pairs_kernel<AddMover1<T>, 2, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, cudaStream_t s)
+{
+    switch (dtype) {
+    case PTOC_F32: return launch_add_t<float>(p, vb, grid, s);
+    case PTOC_I32: return launch_add_t<int32_t>(p, vb, grid, s);
+    case PTOC_F16: return launch_add_t<__half>(p, vb, grid, s);
+    default: return launch_add_t<__nv_bfloat16>(p, vb, grid, s);
+    }
+}
+
+template <class T>
+static int add_occupancy_t(int vb, size_t smem)
+{
+    if (vb == 16) return occupancy_of_kernel(pairs_kernel<AddMover<T, 16>, 16, kAddUnroll>, smem);
+    if (vb == 8) return occupancy_of_kernel(pairs_kernel<AddMover<T, 8>, 8, kAddUnroll>, smem);
+    if (vb == 4) return occupancy_of_kernel(pairs_kernel<AddMover<T, 4>, 4, kAddUnroll>, smem);
+    if constexpr (sizeof(T) == 2) return occupancy_of_kernel(pairs_kernel<AddMover1<T>, 2, kAddUnroll>, smem);
+    return 1;
+}
+
+int pairs_add_blocks_per_sm(int dtype, int vb, int nranks)
+{
+    const size_t smem = a2av_smem_bytes(nranks);
+    switch (dtype) {
+    case PTOC_F32: return add_occupancy_t<float>(vb, smem);
+    case PTOC_I32: return add_occupancy_t<int32_t>(vb, smem);
+    case PTOC_F16: return add_occupancy_t<__half>(vb, smem);
+    default: return add_occupancy_t<__nv_bfloat16>(vb, smem);
+    }
 }
 
 }  // namespace ptoc

@@ -26,12 +26,19 @@ int elem_size(int dtype)
 
 bool valid_dtype(int dtype) { return elem_size(dtype) != 0; }
 
-// op: Sum / Max / Min are implemented; Prod is a reserved ABI value.
+// op of TREDUCE: Sum / Max / Min ([TR] §1.3); Prod belongs to the allreduce
+// family only.
 ptoc_status check_op(int op)
 {
     if (op == PTOC_SUM || op == PTOC_MAX || op == PTOC_MIN) return PTOC_OK;
     if (op == PTOC_PROD) return PTOC_ERR_UNSUPPORTED;
     return PTOC_ERR_INVALID_ARG;
+}
+
+// op of the allreduce family (reduce_scatter, allreduce): all four.
+ptoc_status check_op_allreduce(int op)
+{
+    return (op >= PTOC_SUM && op <= PTOC_PROD) ? PTOC_OK : PTOC_ERR_INVALID_ARG;
 }
 
 // Byte range [lo, hi) a buffer occupies.
@@ -182,7 +189,7 @@ cudaError_t launch_reduce_regs(int dtype, const ReduceParams& p, int op, int vb,
 }
 
 // Tile a [rows, cols] box with pitch ld and launch one reduction over it
-// (p.src, p.dst, p.nranks and p.scatter already filled in): the
+// (p.src, p.dst, p.nranks and p.dst_mode already filled in): the
 // shared-memory pipeline when every address and the pitch are 16-byte
 // aligned, the register kernel otherwise.
 cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, int64_t cols, int64_t ld,
@@ -225,7 +232,8 @@ ptoc_status check_group(const ptoc_group* g, bool need_root)
 
 bool aligned(const void* p, int eb) { return ((uintptr_t)p % (uintptr_t)eb) == 0; }
 
-// Shared checks of the window collectives (reduce_scatter, allgather).
+// Shared checks of the window collectives (reduce_scatter, allgather,
+// allreduce, broadcast): group, dtype, sizes, alignment, disjoint windows.
 ptoc_status check_windows(const ptoc_group* w, int64_t rows, int64_t cols, int64_t ld, int dtype,
                           int64_t* fp_out)
 {
@@ -246,6 +254,59 @@ ptoc_status check_windows(const ptoc_group* w, int64_t rows, int64_t cols, int64
         }
     *fp_out = fp;
     return PTOC_OK;
+}
+
+// Shared checks of the pairwise exchanges over [target_rows, size] buffers
+// (all_to_all_v, all_to_all, the combine). `writes` are the buffers the call
+// writes (each `wbytes` long), `reads` the ones it only reads; outputs must not
+// overlap anything, inputs may overlap each other.
+struct Span {
+    const void* p;
+    uintptr_t bytes;
+};
+
+ptoc_status check_disjoint_outputs(const Span* writes, int nw, const Span* reads, int nr)
+{
+    for (int a = 0; a < nw; ++a) {
+        const Range ra{(uintptr_t)writes[a].p, (uintptr_t)writes[a].p + writes[a].bytes};
+        for (int b = a + 1; b < nw; ++b) {
+            const Range rb{(uintptr_t)writes[b].p, (uintptr_t)writes[b].p + writes[b].bytes};
+            if (overlap(ra, rb)) return PTOC_ERR_ALIAS;
+        }
+        for (int b = 0; b < nr; ++b) {
+            const Range rb{(uintptr_t)reads[b].p, (uintptr_t)reads[b].p + reads[b].bytes};
+            if (overlap(ra, rb)) return PTOC_ERR_ALIAS;
+        }
+    }
+    return PTOC_OK;
+}
+
+// The vector width and tile size of a pairwise exchange, and its launch.
+// `add` selects the combine's add mover (needs the element type).
+ptoc_status launch_pairs(A2avParams& p, const void* const* a, const void* const* b, int n, int eb, int dtype,
+                         bool add, cudaStream_t stream)
+{
+    uintptr_t addr_or = 0;
+    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)a[r] | (uintptr_t)b[r];
+    const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
+    const int unroll = add ? 4 : a2av_unroll();
+    p.tile_bytes = (int64_t)vb * kBlock * unroll;
+    // tile indices are int32 in the kernel
+    const int64_t fp = p.max_recv * n * p.row_bytes;
+    if ((int64_t)n * (fp / p.tile_bytes + 1) + (int64_t)n * n >= INT32_MAX) return PTOC_ERR_UNSUPPORTED;
+    const int per_sm = add ? pairs_add_blocks_per_sm(dtype, vb, n) : a2av_blocks_per_sm(vb, unroll, n);
+    const dim3 grid((unsigned)(sm_count() * per_sm));
+    const cudaError_t e = add ? launch_pairs_add(p, dtype, vb, grid, stream) : launch_a2av(p, vb, unroll, grid, stream);
+    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+ptoc_status check_pair_group(const ptoc_group* a, const ptoc_group* b)
+{
+    ptoc_status st = check_group(a, false);
+    if (st != PTOC_OK) return st;
+    st = check_group(b, false);
+    if (st != PTOC_OK) return st;
+    return a->nranks == b->nranks ? PTOC_OK : PTOC_ERR_INVALID_ARG;
 }
 
 }  // namespace
@@ -295,10 +356,10 @@ extern "C" ptoc_status ptoc_treduce(const ptoc_group* group, void* dst, int64_t 
         if (r != group->root) p.src[k++] = group->tensors[r];
     p.dst[0] = dst;
     p.nranks = n;
-    p.scatter = 0;
+    p.dst_mode = kDstOne;
     // One rank: a bit copy (TREDUCE article §4.3). Max with a single operand
     // is exactly that, NaN payloads included.
-    int eff_op = (n == 1) ? PTOC_MAX : (int)op;
+    const int eff_op = (n == 1) ? PTOC_MAX : (int)op;
 
     // Contiguous valid box (full rows, or a single row): one flat row.
     const bool flat = (valid_cols == ld) || (valid_rows == 1);
@@ -312,31 +373,82 @@ extern "C" ptoc_status ptoc_treduce(const ptoc_group* group, void* dst, int64_t 
     return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }
 
-extern "C" ptoc_status ptoc_reduce_scatter(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
-                                           ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
+// reduce_scatter (dst_mode kDstOwner) and allreduce (kDstAll) over windows.
+static ptoc_status window_reduction(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                                    ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream, int dst_mode)
 {
     int64_t fp = 0;
     ptoc_status st = check_windows(windows, rows, cols, ld, dtype, &fp);
     if (st != PTOC_OK) return st;
-    st = check_op(op);
+    st = check_op_allreduce(op);
     if (st != PTOC_OK) return st;
-    if (rows == 0 || cols == 0) return PTOC_OK;
     const int n = windows->nranks;
+    // Nothing to do: an empty box, or one rank (its window already holds the
+    // reduction of itself).
+    if (rows == 0 || cols == 0 || n == 1) return PTOC_OK;
     const int eb = elem_size(dtype);
 
     ReduceParams p;
     memset(&p, 0, sizeof(p));
     for (int r = 0; r < n; ++r) {
         p.src[r] = windows->tensors[r];     // rank order 0..N-1
-        p.dst[r] = windows->tensors[r];     // window r receives its own chunk
+        p.dst[r] = windows->tensors[r];
     }
     p.nranks = n;
-    p.scatter = 1;
-    const int eff_op = (n == 1) ? PTOC_MAX : (int)op;
+    p.dst_mode = dst_mode;
     uintptr_t addr_or = 0;
     for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)windows->tensors[r];
-    const int vb = pick_vector_bytes(addr_or, ld * eb, eb);
-    cudaError_t e = launch_reduction(dtype, p, eff_op, rows, cols, ld, eb, vb, stream);
+    // allreduce writes every window with the same value: when the windows are
+    // whole rows it is one flat row
+    const bool flat = (dst_mode == kDstAll) && (cols == ld || rows == 1);
+    const int64_t frows = flat ? 1 : rows;
+    const int64_t fcols = flat ? rows * ld - (ld - cols) : cols;
+    const int64_t fld = flat ? fcols : ld;
+    const int vb = pick_vector_bytes(addr_or, flat ? 0 : ld * eb, eb);
+    cudaError_t e = launch_reduction(dtype, p, (int)op, frows, fcols, fld, eb, vb, stream);
+    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+extern "C" ptoc_status ptoc_reduce_scatter(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                                           ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
+{
+    return window_reduction(windows, rows, cols, ld, op, dtype, stream, kDstOwner);
+}
+
+extern "C" ptoc_status ptoc_allreduce(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                                      ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
+{
+    return window_reduction(windows, rows, cols, ld, op, dtype, stream, kDstAll);
+}
+
+// allgather (root < 0: row i comes from its owner window) and broadcast
+// (every row comes from window `root`).
+static ptoc_status window_copy(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                               ptoc_dtype dtype, cudaStream_t stream, int root)
+{
+    const int n = windows->nranks;
+    const int eb = elem_size(dtype);
+    GatherParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) p.win[r] = windows->tensors[r];
+    p.nranks = n;
+    p.root = root;
+    uintptr_t addr_or = 0;
+    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)windows->tensors[r];
+    // broadcast copies the same rows to every window: whole rows are one flat row
+    const bool flat = (root >= 0) && (cols == ld || rows == 1);
+    const int64_t frows = flat ? 1 : rows;
+    const int64_t fcols = flat ? rows * ld - (ld - cols) : cols;
+    const int64_t fld = flat ? fcols : ld;
+    const int vb = pick_vector_bytes(addr_or, flat ? 0 : ld * eb, eb);
+    const Box b = make_box(frows, fcols, fld, eb, vb, kBlock);
+    p.ld = fld;
+    p.rows = frows;
+    p.vpr = b.vpr;
+    p.tail = b.tail;
+    p.tpr = b.tpr;
+    p.ntiles = b.ntiles;
+    cudaError_t e = launch_gather(p, eb, vb, grid_for(p.ntiles), stream);
     return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }
 
@@ -347,25 +459,19 @@ extern "C" ptoc_status ptoc_allgather(const ptoc_group* windows, int64_t rows, i
     ptoc_status st = check_windows(windows, rows, cols, ld, dtype, &fp);
     if (st != PTOC_OK) return st;
     if (rows == 0 || cols == 0 || windows->nranks == 1) return PTOC_OK;
-    const int n = windows->nranks;
-    const int eb = elem_size(dtype);
+    return window_copy(windows, rows, cols, ld, dtype, stream, -1);
+}
 
-    GatherParams p;
-    memset(&p, 0, sizeof(p));
-    for (int r = 0; r < n; ++r) p.win[r] = windows->tensors[r];
-    p.nranks = n;
-    uintptr_t addr_or = 0;
-    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)windows->tensors[r];
-    const int vb = pick_vector_bytes(addr_or, ld * eb, eb);
-    const Box b = make_box(rows, cols, ld, eb, vb, kBlock);
-    p.ld = ld;
-    p.rows = rows;
-    p.vpr = b.vpr;
-    p.tail = b.tail;
-    p.tpr = b.tpr;
-    p.ntiles = b.ntiles;
-    cudaError_t e = launch_gather(p, eb, vb, grid_for(p.ntiles), stream);
-    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+extern "C" ptoc_status ptoc_broadcast(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
+                                      ptoc_dtype dtype, cudaStream_t stream)
+{
+    ptoc_status st = check_group(windows, true);
+    if (st != PTOC_OK) return st;
+    int64_t fp = 0;
+    st = check_windows(windows, rows, cols, ld, dtype, &fp);
+    if (st != PTOC_OK) return st;
+    if (rows == 0 || cols == 0 || windows->nranks == 1) return PTOC_OK;
+    return window_copy(windows, rows, cols, ld, dtype, stream, windows->root);
 }
 
 extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* targets,
@@ -373,11 +479,8 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
                                          int64_t target_rows, int64_t size, ptoc_dtype dtype,
                                          cudaStream_t stream)
 {
-    ptoc_status st = check_group(inputs, false);
+    ptoc_status st = check_pair_group(inputs, targets);
     if (st != PTOC_OK) return st;
-    st = check_group(targets, false);
-    if (st != PTOC_OK) return st;
-    if (inputs->nranks != targets->nranks) return PTOC_ERR_INVALID_ARG;
     if (!send_counts || !recv_counts) return PTOC_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
     if (target_rows < 0 || size < 0) return PTOC_ERR_INVALID_ARG;
@@ -390,46 +493,114 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
         if (!aligned(send_counts[r], 4) || !aligned(recv_counts[r], 4)) return PTOC_ERR_INVALID_ARG;
         if (!aligned(inputs->tensors[r], eb) || !aligned(targets->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
     }
-
-    // Outputs must not overlap anything (the page requires the five operands
-    // to be pairwise-distinct allocations); inputs may share memory.
-    const uintptr_t cb = (uintptr_t)n * 4u;
-    for (int a = 0; a < n; ++a) {
-        const Range ta{(uintptr_t)targets->tensors[a], (uintptr_t)targets->tensors[a] + (uintptr_t)fp};
-        const Range ra{(uintptr_t)recv_counts[a], (uintptr_t)recv_counts[a] + cb};
-        for (int b = 0; b < n; ++b) {
-            const Range ib{(uintptr_t)inputs->tensors[b], (uintptr_t)inputs->tensors[b] + (uintptr_t)fp};
-            const Range sb{(uintptr_t)send_counts[b], (uintptr_t)send_counts[b] + cb};
-            const Range tb{(uintptr_t)targets->tensors[b], (uintptr_t)targets->tensors[b] + (uintptr_t)fp};
-            const Range rb{(uintptr_t)recv_counts[b], (uintptr_t)recv_counts[b] + cb};
-            if (overlap(ta, ib) || overlap(ta, sb) || overlap(ra, ib) || overlap(ra, sb) || overlap(ta, rb))
-                return PTOC_ERR_ALIAS;
-            if (a != b && (overlap(ta, tb) || overlap(ra, rb))) return PTOC_ERR_ALIAS;
-        }
+    // Outputs (targets, recv_counts) must not overlap anything (the page
+    // requires the five operands to be pairwise-distinct allocations); inputs
+    // may share memory.
+    Span writes[2 * kMaxRanks], reads[2 * kMaxRanks];
+    for (int r = 0; r < n; ++r) {
+        writes[r] = Span{targets->tensors[r], (uintptr_t)fp};
+        writes[n + r] = Span{recv_counts[r], (uintptr_t)n * 4u};
+        reads[r] = Span{inputs->tensors[r], (uintptr_t)fp};
+        reads[n + r] = Span{send_counts[r], (uintptr_t)n * 4u};
     }
+    st = check_disjoint_outputs(writes, 2 * n, reads, 2 * n);
+    if (st != PTOC_OK) return st;
 
     A2avParams p;
     memset(&p, 0, sizeof(p));
     for (int r = 0; r < n; ++r) {
         p.in[r] = inputs->tensors[r];
-        p.tgt[r] = targets->tensors[r];
-        p.sc[r] = send_counts[r];
-        p.rc[r] = recv_counts[r];
+        p.out[r] = targets->tensors[r];
+        p.cnt[r] = send_counts[r];
+        p.pub[r] = recv_counts[r];
     }
     p.nranks = n;
     p.max_recv = target_rows / n;
     p.row_bytes = size * eb;
-    uintptr_t addr_or = 0;
-    for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)inputs->tensors[r] | (uintptr_t)targets->tensors[r];
-    const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
-    const int unroll = a2av_unroll();
-    p.tile_bytes = (int64_t)vb * kBlock * unroll;
-    // tile indices are int32 in the kernel
-    if ((int64_t)n * fp / p.tile_bytes + (int64_t)n * n >= INT32_MAX) return PTOC_ERR_UNSUPPORTED;
-    const int per_sm = a2av_blocks_per_sm(vb, unroll, n);
-    dim3 grid((unsigned)(sm_count() * per_sm));
-    cudaError_t e = launch_a2av(p, vb, unroll, grid, stream);
-    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+    p.full = 0;
+    p.publish = 1;
+    return launch_pairs(p, inputs->tensors, targets->tensors, n, eb, dtype, false, stream);
+}
+
+extern "C" ptoc_status ptoc_all_to_all(const ptoc_group* inputs, const ptoc_group* targets,
+                                       int64_t target_rows, int64_t size, ptoc_dtype dtype, cudaStream_t stream)
+{
+    ptoc_status st = check_pair_group(inputs, targets);
+    if (st != PTOC_OK) return st;
+    if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
+    if (target_rows < 0 || size < 0) return PTOC_ERR_INVALID_ARG;
+    const int n = inputs->nranks;
+    const int eb = elem_size(dtype);
+    const int64_t fp = footprint(target_rows, size, size, eb);
+    if (fp < 0) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r)
+        if (!aligned(inputs->tensors[r], eb) || !aligned(targets->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
+    Span writes[kMaxRanks], reads[kMaxRanks];
+    for (int r = 0; r < n; ++r) {
+        writes[r] = Span{targets->tensors[r], (uintptr_t)fp};
+        reads[r] = Span{inputs->tensors[r], (uintptr_t)fp};
+    }
+    st = check_disjoint_outputs(writes, n, reads, n);
+    if (st != PTOC_OK) return st;
+    const int64_t chunk = target_rows / n;
+    if (chunk == 0 || size == 0) return PTOC_OK;
+
+    A2avParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) {
+        p.in[r] = inputs->tensors[r];
+        p.out[r] = targets->tensors[r];
+    }
+    p.nranks = n;
+    p.max_recv = chunk;
+    p.row_bytes = size * eb;
+    p.full = 1;
+    p.publish = 0;
+    return launch_pairs(p, inputs->tensors, targets->tensors, n, eb, dtype, false, stream);
+}
+
+extern "C" ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, const ptoc_group* outputs,
+                                                 const int32_t* const* recv_counts, int64_t target_rows,
+                                                 int64_t size, ptoc_atomic_type atomic, ptoc_dtype dtype,
+                                                 cudaStream_t stream)
+{
+    ptoc_status st = check_pair_group(windows, outputs);
+    if (st != PTOC_OK) return st;
+    if (!recv_counts) return PTOC_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
+    if (atomic != PTOC_ATOMIC_NONE && atomic != PTOC_ATOMIC_ADD) return PTOC_ERR_INVALID_ARG;
+    if (target_rows < 0 || size < 0) return PTOC_ERR_INVALID_ARG;
+    const int n = windows->nranks;
+    const int eb = elem_size(dtype);
+    const int64_t fp = footprint(target_rows, size, size, eb);
+    if (fp < 0) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r) {
+        if (!recv_counts[r] || !aligned(recv_counts[r], 4)) return PTOC_ERR_INVALID_ARG;
+        if (!aligned(windows->tensors[r], eb) || !aligned(outputs->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
+    }
+    Span writes[kMaxRanks], reads[2 * kMaxRanks];
+    for (int r = 0; r < n; ++r) {
+        writes[r] = Span{outputs->tensors[r], (uintptr_t)fp};
+        reads[r] = Span{windows->tensors[r], (uintptr_t)fp};
+        reads[n + r] = Span{recv_counts[r], (uintptr_t)n * 4u};
+    }
+    st = check_disjoint_outputs(writes, n, reads, 2 * n);
+    if (st != PTOC_OK) return st;
+    if (target_rows / n == 0 || size == 0) return PTOC_OK;
+
+    A2avParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) {
+        p.in[r] = windows->tensors[r];      // pair (a = d, b = s): window d -> output s
+        p.out[r] = outputs->tensors[r];
+        p.cnt[r] = recv_counts[r];
+    }
+    p.nranks = n;
+    p.max_recv = target_rows / n;
+    p.row_bytes = size * eb;
+    p.full = 0;
+    p.publish = 0;
+    return launch_pairs(p, windows->tensors, outputs->tensors, n, eb, dtype, atomic == PTOC_ATOMIC_ADD, stream);
 }
 
 extern "C" const char* ptoc_status_string(ptoc_status s)

@@ -14,7 +14,11 @@ constexpr int kMaxRanks = PTOC_MAX_RANKS;
 constexpr int kBlock = 256;          // threads per CTA for every streaming kernel
 constexpr int kMaxDevices = 64;      // per-device caches
 
-enum Op : int { kSum = 0, kMax = 1, kMin = 2 };
+enum Op : int { kSum = 0, kMax = 1, kMin = 2, kProd = 3 };
+
+// Where a reduction writes: one dst, the owner window of each row
+// (reduce_scatter), or every window (allreduce).
+enum DstMode : int { kDstOne = 0, kDstOwner = 1, kDstAll = 2 };
 
 // Shapes of the shared-memory-pipelined reduction: S stages of G ranks, CTAs
 // of B threads (one tile = B vectors of 16 bytes). Shared memory per CTA is
@@ -31,7 +35,7 @@ constexpr size_t async_smem_bytes(int cfg) { return (size_t)kAsyncS[cfg] * kAsyn
 // kBlock * U vectors (the last segment of a row also owns the tail).
 struct ReduceParams {
     const void* src[kMaxRanks];   // sources in reduction order (root first)
-    void* dst[kMaxRanks];         // dst[0] for TREDUCE; window r for reduce_scatter
+    void* dst[kMaxRanks];         // dst[0] for TREDUCE; window r for reduce_scatter / allreduce
     int64_t ld;                   // row pitch, elements
     int64_t rows;                 // rows of the box (also the scatter chunk basis)
     int64_t vpr;                  // full vectors per row
@@ -39,28 +43,41 @@ struct ReduceParams {
     int64_t ntiles;               // rows * tpr
     int32_t tail;                 // elements after the last full vector of a row
     int32_t nranks;
-    int32_t scatter;              // 1: row i is written to dst[owner(i)]
+    int32_t dst_mode;             // DstMode
 };
 
-// allgather: same box description; win[r] is rank r's window.
+// allgather / broadcast: same box description; win[r] is rank r's window.
+// Row i is read from win[owner(i)] (allgather) or from win[root] when
+// root >= 0 (broadcast), and written to every other window.
 struct GatherParams {
     void* win[kMaxRanks];
     int64_t ld, rows, vpr, tpr, ntiles;
-    int32_t tail, nranks;
+    int32_t tail, nranks, root;
 };
 
-// all_to_all_v: one contiguous segment per (s, d) pair, cut into tiles of
-// tile_bytes; clamped counts and tile prefix sums over pairs are built in
-// shared memory per CTA (int32: a launch moves fewer than 2^31 tiles).
+// Pairwise exchanges over the flat [N * MAX_RECV, size] layout. Pair (a, b)
+// moves count(a, b) rows from in[a] rows [b * MAX_RECV, ..) to out[b] rows
+// [a * MAX_RECV, ..):
+//   all_to_all_v : a = sender, b = destination, count = clamp(cnt[a][b]) with
+//                  cnt = send_counts; publishes pub[b][a] = count.
+//   all_to_all   : count = MAX_RECV for every pair (cnt unused).
+//   combine      : a = the rank that received, b = the original sender,
+//                  count = clamp(cnt[a][b]) with cnt = recv_counts; out is
+//                  overwritten or added into (AtomicType).
+// Each pair is one contiguous segment cut into tiles of tile_bytes; clamped
+// counts and tile prefix sums over pairs are built in shared memory per CTA
+// (int32: a launch moves fewer than 2^31 tiles).
 struct A2avParams {
     const void* in[kMaxRanks];
-    void* tgt[kMaxRanks];
-    const int32_t* sc[kMaxRanks];
-    int32_t* rc[kMaxRanks];
+    void* out[kMaxRanks];
+    const int32_t* cnt[kMaxRanks];
+    int32_t* pub[kMaxRanks];
     int64_t max_recv;             // target_rows / nranks
     int64_t row_bytes;            // size * element bytes
     int64_t tile_bytes;
     int32_t nranks;
+    int32_t full;                 // 1: every count is MAX_RECV
+    int32_t publish;              // 1: write pub[b][a]
 };
 
 // Launchers (one translation unit per element type for the reductions).
@@ -72,6 +89,10 @@ cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, int unroll,
 cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s);
+// The combine with AtomicType kAdd: out += in per element (binary32 for
+// floating types, one RNE narrowing; int32 wraps).
+cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, cudaStream_t s);
+int pairs_add_blocks_per_sm(int dtype, int vb, int nranks);
 
 // Shared-memory-pipelined reduction (16-byte-aligned data): persistent grid.
 cudaError_t launch_async_f32(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);

@@ -1,4 +1,4 @@
-// TREDUCE / reduce_scatter, pipelined through shared memory.
+// TREDUCE / reduce_scatter / allreduce, pipelined through shared memory.
 //
 // Same arithmetic as reduce_kernel (root first, then ascending ranks; binary32
 // accumulation; raw-encoding select for 16-bit Max / Min). What differs is how
@@ -121,7 +121,6 @@ __global__ void __launch_bounds__(B, 512 / B) reduce_async_kernel(const __grid_c
         issue();
         cp_async_wait<S - 1>();          // this thread's copies of item i have landed
         const int64_t v = out.seg * B + threadIdx.x;
-        char* dst_base = (char*)(p.scatter ? p.dst[row_owner(out.row, n, p.rows)] : p.dst[0]);
         const bool last_group = (out.g == ngroups - 1);
         if (v < p.vpr) {
             const uint4* slot = stage + (size_t)out_slot * G * B + threadIdx.x;
@@ -135,13 +134,13 @@ __global__ void __launch_bounds__(B, 512 / B) reduce_async_kernel(const __grid_c
                 }
             }
             if (last_group)
-                store_words<4>(dst_base + out.row * p.ld * (int64_t)sizeof(T) + v * 16, acc.out());
+                store_result<4>(p, out.row, out.row * p.ld * (int64_t)sizeof(T) + v * 16, acc.out());
         }
         if (last_group && p.tail > 0 && out.seg == p.tpr - 1) {
             using Raw = typename Scalar<T>::Raw;
             for (int c = threadIdx.x; c < p.tail; c += B) {
                 const int64_t e = out.row * p.ld + p.vpr * VE + c;
-                reinterpret_cast<Raw*>(dst_base)[e] = reduce_one<T, OP>(p, e);
+                store_elem<Raw>(p, out.row, e, reduce_one<T, OP>(p, e));
             }
         }
         cursor_next(out, p, ngroups, dq, dr);
@@ -204,6 +203,7 @@ cudaError_t launch_async_t(const ReduceParams& p, int op, int cfg, int grid, cud
     switch (op) {
     case kSum: return launch_async_op<T, kSum>(p, cfg, grid, s);
     case kMax: return launch_async_op<T, kMax>(p, cfg, grid, s);
+    case kProd: return launch_async_op<T, kProd>(p, cfg, grid, s);
     default: return launch_async_op<T, kMin>(p, cfg, grid, s);
     }
 }
@@ -214,6 +214,7 @@ int async_occupancy_t(int op, int cfg)
     switch (op) {
     case kSum: return async_occupancy_op<T, kSum>(cfg);
     case kMax: return async_occupancy_op<T, kMax>(cfg);
+    case kProd: return async_occupancy_op<T, kProd>(cfg);
     default: return async_occupancy_op<T, kMin>(cfg);
     }
 }

@@ -1,4 +1,4 @@
-// TREDUCE / reduce_scatter kernels for int32_t elements (one translation unit
+// TREDUCE / reduce_scatter / allreduce kernels for int32_t elements (one translation unit
 // per element type so the library builds in parallel).
 #include <atomic>
 
@@ -23,8 +23,8 @@ cudaError_t launch_async_i32(const ReduceParams& p, int op, int cfg, int grid, c
 // first query of a device also opts the kernel into its shared-memory size.
 int occupancy_async_i32(int op, int cfg, int dev)
 {
-    static std::atomic<int> cache[kMaxDevices][3][kAsyncCfgs];
-    if (dev < 0 || dev >= kMaxDevices || op < 0 || op > 2 || cfg < 0 || cfg >= kAsyncCfgs)
+    static std::atomic<int> cache[kMaxDevices][4][kAsyncCfgs];
+    if (dev < 0 || dev >= kMaxDevices || op < 0 || op > 3 || cfg < 0 || cfg >= kAsyncCfgs)
         return async_occupancy_t<int32_t>(op, cfg);
     int v = cache[dev][op][cfg].load(std::memory_order_relaxed);
     if (v == 0) {

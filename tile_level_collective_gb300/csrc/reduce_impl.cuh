@@ -1,10 +1,13 @@
-// TREDUCE / reduce_scatter kernel template.
+// TREDUCE / reduce_scatter / allreduce kernel template.
 //
 // What it computes (TREDUCE article, "CANN PTO-ISA TREDUCE 指令详解", §1.1,
 // §4.3): for every element of the valid box, acc = src[root]; then for every
 // other rank in ascending order acc = acc (+) src[r]; store. The host passes
 // the sources already in that order (src[0] is the root), so the kernel only
-// walks src[0..n-1].
+// walks src[0..n-1]. (+) is Sum, Max, Min, or Prod (the allreduce family's
+// kProd, "Distributed Operators (N6)", ABI enums). The result goes to one
+// dst (TREDUCE), to the window that owns the row (reduce_scatter) or to every
+// window (allreduce).
 //
 // How (GB300 design, not the page's UB ping-pong): the op is HBM-bound
 // (N reads + 1 write per element, at most one ALU op per loaded element), so
@@ -138,6 +141,7 @@ struct VecAcc<float, OP, W> {
         for (int i = 0; i < W; ++i) {
             const float v = __uint_as_float(x.w[i]);
             if constexpr (OP == kSum) a[i] = __fadd_rn(a[i], v);
+            else if constexpr (OP == kProd) a[i] = __fmul_rn(a[i], v);
             else if constexpr (OP == kMax) a[i] = (v > a[i]) ? v : a[i];
             else a[i] = (v < a[i]) ? v : a[i];
         }
@@ -164,6 +168,7 @@ struct VecAcc<int32_t, OP, W> {
 #pragma unroll
         for (int i = 0; i < W; ++i) {
             if constexpr (OP == kSum) a[i] = a[i] + x.w[i];   // wraps modulo 2^32
+            else if constexpr (OP == kProd) a[i] = a[i] * x.w[i];   // wraps modulo 2^32
             else if constexpr (OP == kMax) a[i] = ((int32_t)x.w[i] > (int32_t)a[i]) ? x.w[i] : a[i];
             else a[i] = ((int32_t)x.w[i] < (int32_t)a[i]) ? x.w[i] : a[i];
         }
@@ -177,8 +182,8 @@ struct VecAcc<int32_t, OP, W> {
     }
 };
 
-// 16-bit Sum: each word holds two elements (low half = lower address);
-// widened exactly to binary32, accumulated there, narrowed with RNE.
+// 16-bit Sum / Prod: each word holds two elements (low half = lower
+// address); widened exactly to binary32, accumulated there, narrowed with RNE.
 template <class T>
 struct Pair16;
 template <>
@@ -216,7 +221,7 @@ struct Pair16<__nv_bfloat16> {
     }
 };
 
-template <class T, int W>
+template <class T, int W, int OP = kSum>
 struct Acc16Sum {
     float a[2 * W];
     __device__ __forceinline__ void init(const Words<W>& x)
@@ -233,8 +238,13 @@ struct Acc16Sum {
 #pragma unroll
         for (int i = 0; i < W; ++i) {
             const float2 f = Pair16<T>::widen(x.w[i]);
-            a[2 * i] = __fadd_rn(a[2 * i], f.x);
-            a[2 * i + 1] = __fadd_rn(a[2 * i + 1], f.y);
+            if constexpr (OP == kProd) {
+                a[2 * i] = __fmul_rn(a[2 * i], f.x);
+                a[2 * i + 1] = __fmul_rn(a[2 * i + 1], f.y);
+            } else {
+                a[2 * i] = __fadd_rn(a[2 * i], f.x);
+                a[2 * i + 1] = __fadd_rn(a[2 * i + 1], f.y);
+            }
         }
     }
     __device__ __forceinline__ Words<W> out() const
@@ -276,9 +286,11 @@ struct Acc16Sel {
 };
 
 template <int W> struct VecAcc<__half, kSum, W> : Acc16Sum<__half, W> {};
+template <int W> struct VecAcc<__half, kProd, W> : Acc16Sum<__half, W, kProd> {};
 template <int W> struct VecAcc<__half, kMax, W> : Acc16Sel<__half, kMax, W> {};
 template <int W> struct VecAcc<__half, kMin, W> : Acc16Sel<__half, kMin, W> {};
 template <int W> struct VecAcc<__nv_bfloat16, kSum, W> : Acc16Sum<__nv_bfloat16, W> {};
+template <int W> struct VecAcc<__nv_bfloat16, kProd, W> : Acc16Sum<__nv_bfloat16, W, kProd> {};
 template <int W> struct VecAcc<__nv_bfloat16, kMax, W> : Acc16Sel<__nv_bfloat16, kMax, W> {};
 template <int W> struct VecAcc<__nv_bfloat16, kMin, W> : Acc16Sel<__nv_bfloat16, kMin, W> {};
 
@@ -319,6 +331,7 @@ __device__ __forceinline__ typename Scalar<T>::Raw reduce_one(const ReduceParams
         for (int r = 1; r < n; ++r) {
             const float v = __uint_as_float(reinterpret_cast<const Raw*>(p.src[r])[e]);
             if constexpr (OP == kSum) a = __fadd_rn(a, v);
+            else if constexpr (OP == kProd) a = __fmul_rn(a, v);
             else if constexpr (OP == kMax) a = (v > a) ? v : a;
             else a = (v < a) ? v : a;
         }
@@ -327,6 +340,7 @@ __device__ __forceinline__ typename Scalar<T>::Raw reduce_one(const ReduceParams
         for (int r = 1; r < n; ++r) {
             const uint32_t v = reinterpret_cast<const Raw*>(p.src[r])[e];
             if constexpr (OP == kSum) acc = acc + v;
+            else if constexpr (OP == kProd) acc = acc * v;
             else if constexpr (OP == kMax) acc = ((int32_t)v > (int32_t)acc) ? v : acc;
             else acc = ((int32_t)v < (int32_t)acc) ? v : acc;
         }
@@ -338,12 +352,14 @@ __device__ __forceinline__ typename Scalar<T>::Raw reduce_one(const ReduceParams
             const float v = Scalar<T>::widen(raw);
             if constexpr (OP == kSum) {
                 a = __fadd_rn(a, v);
+            } else if constexpr (OP == kProd) {
+                a = __fmul_rn(a, v);
             } else if ((OP == kMax && v > a) || (OP == kMin && v < a)) {
                 a = v;
                 acc = raw;
             }
         }
-        if constexpr (OP == kSum) return Scalar<T>::narrow(a);
+        if constexpr (OP == kSum || OP == kProd) return Scalar<T>::narrow(a);
         return acc;
     }
 }
@@ -353,6 +369,35 @@ __device__ __forceinline__ typename Scalar<T>::Raw reduce_one(const ReduceParams
 __device__ __forceinline__ int row_owner(int64_t row, int n, int64_t rows)
 {
     return (int)(((row + 1) * (int64_t)n - 1) / rows);
+}
+
+// The one destination of a row (kDstOne, kDstOwner); kDstAll rows go to every
+// window and use store_all / put_all instead.
+__device__ __forceinline__ char* row_dst(const ReduceParams& p, int64_t row)
+{
+    return (char*)(p.dst_mode == kDstOwner ? p.dst[row_owner(row, p.nranks, p.rows)] : p.dst[0]);
+}
+
+// Store one result vector at byte offset `off` of its destination(s).
+template <int W>
+__device__ __forceinline__ void store_result(const ReduceParams& p, int64_t row, int64_t off, const Words<W>& v)
+{
+    if (p.dst_mode == kDstAll) {
+        for (int r = 0; r < p.nranks; ++r) store_words<W>((char*)p.dst[r] + off, v);
+    } else {
+        store_words<W>(row_dst(p, row) + off, v);
+    }
+}
+
+// Store one result element at element offset `e` of its destination(s).
+template <class Raw>
+__device__ __forceinline__ void store_elem(const ReduceParams& p, int64_t row, int64_t e, Raw v)
+{
+    if (p.dst_mode == kDstAll) {
+        for (int r = 0; r < p.nranks; ++r) reinterpret_cast<Raw*>(p.dst[r])[e] = v;
+    } else {
+        reinterpret_cast<Raw*>(row_dst(p, row))[e] = v;
+    }
 }
 
 // ---- the kernel --------------------------------------------------------------
@@ -369,7 +414,6 @@ __device__ __forceinline__ void reduce_vectors(const ReduceParams& p)
         const int64_t row = t / p.tpr;
         const int64_t seg = t - row * p.tpr;
         const int64_t row_elem = row * p.ld;
-        char* dst_base = (char*)(p.scatter ? p.dst[row_owner(row, n, p.rows)] : p.dst[0]);
         const int64_t v0 = seg * TV + threadIdx.x;
 
         // byte offsets of this thread's U vectors (negative = inactive)
@@ -412,7 +456,7 @@ __device__ __forceinline__ void reduce_vectors(const ReduceParams& p)
         }
 #pragma unroll
         for (int k = 0; k < U; ++k)
-            if (off[k] >= 0) store_words<W>(dst_base + off[k], acc[k].out());
+            if (off[k] >= 0) store_result<W>(p, row, off[k], acc[k].out());
 
         // trailing elements of the row (fewer than one vector), owned by the
         // row's last segment
@@ -420,7 +464,7 @@ __device__ __forceinline__ void reduce_vectors(const ReduceParams& p)
             using Raw = typename Scalar<T>::Raw;
             for (int c = threadIdx.x; c < p.tail; c += kBlock) {
                 const int64_t e = row_elem + p.vpr * VE + c;
-                reinterpret_cast<Raw*>(dst_base)[e] = reduce_one<T, OP>(p, e);
+                store_elem<Raw>(p, row, e, reduce_one<T, OP>(p, e));
             }
         }
     }
@@ -435,13 +479,12 @@ __device__ __forceinline__ void reduce_elements(const ReduceParams& p)
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const int64_t row = t / p.tpr;
         const int64_t seg = t - row * p.tpr;
-        Raw* dst_base = (Raw*)(p.scatter ? p.dst[row_owner(row, p.nranks, p.rows)] : p.dst[0]);
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t v = seg * TV + threadIdx.x + (int64_t)k * kBlock;
             if (v < p.vpr) {
                 const int64_t e = row * p.ld + v;
-                dst_base[e] = reduce_one<T, OP>(p, e);
+                store_elem<Raw>(p, row, e, reduce_one<T, OP>(p, e));
             }
         }
     }
@@ -484,6 +527,7 @@ cudaError_t launch_reduce_t(const ReduceParams& p, int op, int vb, int unroll, d
     switch (op) {
     case kSum: return launch_reduce_op<T, kSum>(p, vb, unroll, grid, s);
     case kMax: return launch_reduce_op<T, kMax>(p, vb, unroll, grid, s);
+    case kProd: return launch_reduce_op<T, kProd>(p, vb, unroll, grid, s);
     default: return launch_reduce_op<T, kMin>(p, vb, unroll, grid, s);
     }
 }
@@ -506,6 +550,7 @@ int occupancy_t(int op, int vb, int unroll)
     return unroll == 2 ? occupancy_of<T, OPV, 4, 2>() : occupancy_of<T, OPV, 4, 1>();
     if (op == kSum) { PTOC_OCC(kSum) }
     if (op == kMax) { PTOC_OCC(kMax) }
+    if (op == kProd) { PTOC_OCC(kProd) }
     PTOC_OCC(kMin)
 #undef PTOC_OCC
 }
