@@ -55,7 +55,13 @@ class L2Flush:
         import torch
         self.a.fill_(k & 0xFF)
         torch.amax(self.b, dim=0, out=self.sink)
-KERNEL_SOURCE_DIRS = ["tile_level_collective_gb300/csrc", "include"]
+# The sources each workload's dominant kernel is built and launched from: a
+# recorded ncu traffic figure stays valid while these hash the same.
+_CSRC = "tile_level_collective_gb300/csrc/"
+_COMMON = [_CSRC + "ptoc_api.cu", _CSRC + "ptoc_internal.h", _CSRC + "reduce_impl.cuh", "include/ptoc.h"]
+REDUCE_SOURCES = _COMMON + [_CSRC + f for f in ("reduce_async.cuh", "reduce_f32.cu", "reduce_f16.cu",
+                                                "reduce_bf16.cu", "reduce_i32.cu")]
+MOVE_SOURCES = _COMMON + [_CSRC + "movement.cu"]
 
 
 # ---------------------------------------------------------------------------
@@ -69,9 +75,14 @@ class Workload:
     dtype_compute = "f32"
     storage = ""
     kernel = ""
+    sources = REDUCE_SOURCES      # of the dominant kernel
 
     def config(self):
         raise NotImplementedError
+
+    def prepare(self):
+        """Called before every step, outside the timed events (restores the
+        inputs of in-place workloads)."""
 
 
 class TreduceBench(Workload):
@@ -195,6 +206,11 @@ class RsAgBench(Workload):
 
     def setup_device(self, dev):
         self.dev = [_to_dev(h, dev) for h in self.host]
+        self.saved = [t.clone() for t in self.dev]
+
+    def prepare(self):
+        for t, s in zip(self.dev, self.saved):
+            t.copy_(s)
 
     def launch(self, i, srcs=None, dst=None):
         import tile_level_collective_gb300 as P
@@ -260,8 +276,9 @@ class A2avBench(Workload):
         self.cfg = synth.CONFIG5
         self.name = "all_to_all_v_n16_bf16_7168_maxrecv1536"
         self.storage = "bf16"
-        self.kernel = "a2av_kernel"
+        self.kernel = "pairs_kernel<CopyMover>"
         self.dtype_compute = "u16"
+        self.sources = MOVE_SOURCES
 
     def setup_host(self):
         import numpy as np
@@ -349,6 +366,212 @@ class A2avBench(Workload):
         return 16.0 / max(dt, 1e-9)
 
 
+class WindowOpBench(Workload):
+    """allreduce (Sum) or broadcast (root 0) in place over 8 fp16 windows
+    [8192, 4096] (the reduce_scatter / allgather shapes)."""
+
+    def __init__(self, op):
+        import synth
+        self.op = op
+        self.cfg = synth.CONFIG4
+        self.name = "%s_n8_f16_8192x4096" % op
+        self.storage = "f16"
+        self.kernel = ("reduce_async_kernel<f16> (all-windows mode)" if op == "allreduce"
+                       else "gather_kernel (fixed source window)")
+        self.sources = REDUCE_SOURCES if op == "allreduce" else MOVE_SOURCES
+        self.dtype_compute = "f32" if op == "allreduce" else "u16"
+
+    def bytes_per_launch(self):
+        c = self.cfg
+        elems = c["rows"] * c["cols"]
+        n = c["nranks"]
+        # allreduce: N reads + N writes per element; broadcast: 1 read + N-1 writes
+        return (2 * n if self.op == "allreduce" else n) * 2 * elems
+
+    def launches_per_step(self):
+        return 1
+
+    def bytes_per_step(self):
+        return self.bytes_per_launch()
+
+    def setup_host(self):
+        import synth
+        self.host = [synth.window(r, self.cfg) for r in range(self.cfg["nranks"])]
+
+    def setup_device(self, dev):
+        self.dev = [_to_dev(h, dev) for h in self.host]
+        self.saved = [t.clone() for t in self.dev]
+
+    def prepare(self):
+        for t, s in zip(self.dev, self.saved):
+            t.copy_(s)
+
+    def launch(self, i, srcs=None, dst=None):
+        import tile_level_collective_gb300 as P
+        c = self.cfg
+        wins = srcs or self.dev
+        if self.op == "allreduce":
+            P.ptoc_allreduce(wins, c["rows"], c["cols"], c["ld"], P.SUM, P.F16)
+        else:
+            P.ptoc_broadcast(wins, c["rows"], c["cols"], c["ld"], P.F16, root=0)
+
+    def setup_e2e(self, dev):
+        import torch
+        self.pinned = [_pin(h) for h in self.host]
+        self.out_pinned = [torch.empty(_nbytes(h), dtype=torch.uint8).pin_memory() for h in self.host]
+        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+
+    def e2e_step(self):
+        for d, h in zip(self.e2e_dev, self.pinned):
+            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+        self.launch(0, srcs=self.e2e_dev)
+        for d, o in zip(self.e2e_dev, self.out_pinned):
+            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def d2h_bytes(self):
+        return sum(_nbytes(h) for h in self.host)
+
+    def config(self):
+        c = self.cfg
+        return {"workload": self.name, "op": self.op, "nranks": c["nranks"], "storage_dtype": "f16",
+                "shape": [c["rows"], c["cols"]], "ld": c["ld"], "values": "normal(0,1)",
+                "step": "one in-place %s (inputs restored before every step, outside the timed events)" % self.op,
+                "bytes_per_step": self.bytes_per_step(), "l2": L2_NOTE}
+
+    def oracle_sample(self, rows):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        rows = max(1, min(rows, c["rows"]))
+        wins = [np.ascontiguousarray(h[:rows]) for h in self.host]
+        t0 = time.perf_counter()
+        if self.op == "allreduce":
+            oracle.allreduce(wins, rows, c["cols"], c["ld"], oracle.SUM, oracle.F16)
+        else:
+            oracle.broadcast(wins, 0, rows, c["cols"], c["ld"], oracle.F16)
+        dt = time.perf_counter() - t0
+        n = c["nranks"]
+        nb = (2 * n if self.op == "allreduce" else n) * 2 * rows * c["cols"]
+        return nb, dt, "%s over rows 0..%d of the 8 windows" % (self.op, rows - 1)
+
+    def oracle_rows_per_second(self):
+        nb, dt, _ = self.oracle_sample(64)
+        return 64.0 / max(dt, 1e-9)
+
+
+class PairsBench(A2avBench):
+    """The symmetric all_to_all (every count = MAX_RECV), or the all_to_all_v
+    combine with AtomicType kAdd (the return leg of the dispatch workload:
+    bf16 rows added into the senders' outputs), on the MoE dispatch shapes."""
+
+    def __init__(self, op):
+        super().__init__()
+        self.op = op
+        self.name = ("all_to_all_n16_bf16_7168_chunk1536" if op == "all_to_all"
+                     else "all_to_all_v_combine_add_n16_bf16_7168_maxrecv1536")
+        self.kernel = "pairs_kernel<CopyMover>" if op == "all_to_all" else "pairs_kernel<AddMover<bf16>>"
+        self.dtype_compute = "u16" if op == "all_to_all" else "f32"
+
+    def setup_host(self):
+        import numpy as np
+        import synth
+        super().setup_host()
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        if self.op == "all_to_all":
+            self.moved_rows = n * n * self.mr
+        else:
+            # dispatch values are normal bf16 (added, so they should be numbers)
+            self.host = [synth.values(("normal", 0, 0), synth.DT_BF16, 1234 + s, tr * size).reshape(tr, size)
+                         for s in range(n)]
+            self.out_host = [synth.values(("normal", 0, 0), synth.DT_BF16, 5678 + s, tr * size).reshape(tr, size)
+                             for s in range(n)]
+
+    def bytes_per_launch(self):
+        n = self.cfg["nranks"]
+        row = 2 * self.cfg["size"]
+        if self.op == "all_to_all":
+            return 2 * row * self.moved_rows
+        # combine with kAdd: read the window row, read and write the output row
+        return 3 * row * self.moved_rows + 4 * n * n
+
+    def setup_device(self, dev):
+        import torch
+        import tile_level_collective_gb300 as P
+        super().setup_device(dev)
+        c = self.cfg
+        if self.op == "combine":
+            P.ptoc_all_to_all_v(self.dev, self.d_tg, self.d_sc, self.d_rc, c["target_rows"], c["size"], P.BF16)
+            self.d_out = [_to_dev(o, dev) for o in self.out_host]
+            self.saved = [t.clone() for t in self.d_out]
+            torch.cuda.synchronize()
+
+    def prepare(self):
+        if self.op == "combine":
+            for t, s in zip(self.d_out, self.saved):
+                t.copy_(s)
+
+    def launch(self, i, srcs=None, dst=None):
+        import tile_level_collective_gb300 as P
+        c = self.cfg
+        if self.op == "all_to_all":
+            P.ptoc_all_to_all(srcs or self.dev, self.d_tg, c["target_rows"], c["size"], P.BF16)
+        else:
+            P.ptoc_all_to_all_v_combine(srcs or self.d_tg, self.d_out, self.d_rc, c["target_rows"], c["size"],
+                                        P.ATOMIC_ADD, P.BF16)
+
+    def setup_e2e(self, dev):
+        import torch
+        super().setup_e2e(dev)
+        if self.op == "combine":
+            self.pinned = [_pin(t.cpu().numpy()) for t in self.d_tg]
+
+    def e2e_step(self):
+        for d, h in zip(self.e2e_dev, self.pinned):
+            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+        self.launch(0, srcs=self.e2e_dev)
+        outs = self.d_tg if self.op == "all_to_all" else self.d_out
+        for d, o in zip(outs, self.out_pinned):
+            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+
+    def config(self):
+        c = dict(super().config())
+        c["workload"] = self.name
+        c["op"] = self.op if self.op == "all_to_all" else "all_to_all_v_combine (AtomicType kAdd)"
+        if self.op == "all_to_all":
+            c.pop("send_counts", None)
+            c["chunk_rows"] = self.mr
+        c["moved_rows"] = self.moved_rows
+        c["bytes_per_step"] = self.bytes_per_step()
+        return c
+
+    def oracle_sample(self, rows):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        n, size = c["nranks"], c["size"]
+        mr = max(1, min(rows, self.mr))
+        tr = mr * n
+        ins = [np.ascontiguousarray(h.reshape(n, self.mr, size)[:, :mr].reshape(tr, size)) for h in self.host]
+        if self.op == "all_to_all":
+            tg = [np.empty((tr, size), dtype=np.uint16) for _ in range(n)]
+            t0 = time.perf_counter()
+            oracle.all_to_all(ins, tg, tr, size, 2)
+            dt = time.perf_counter() - t0
+            return 4 * size * n * n * mr, dt, "all_to_all with chunks of %d rows" % mr
+        outs = [np.ascontiguousarray(h.reshape(n, self.mr, size)[:, :mr].reshape(tr, size)) for h in self.out_host]
+        rc = [np.clip(np.array(x), 0, self.mr).astype(np.int32) * mr // self.mr for x in self.sc]
+        rc = [np.ascontiguousarray(np.array([rc[s][d] for s in range(n)], np.int32)) for d in range(n)]
+        t0 = time.perf_counter()
+        oracle.all_to_all_v_combine(ins, outs, rc, tr, size, oracle.ATOMIC_ADD, oracle.BF16)
+        dt = time.perf_counter() - t0
+        moved = sum(int(x.sum()) for x in rc)
+        return 6 * size * moved, dt, "the kAdd combine with capacity %d rows per pair (counts scaled)" % mr
+
+
 def make_workload(name, rows_div=1):
     """The named workload; rows_div > 1 divides its row counts (a smaller case
     of the same kernel, for profiler captures)."""
@@ -366,6 +589,10 @@ def make_workload(name, rows_div=1):
         wl = RsAgBench()
     elif name == "a2av":
         wl = A2avBench()
+    elif name in ("allreduce", "broadcast"):
+        wl = WindowOpBench(name)
+    elif name in ("all_to_all", "combine"):
+        wl = PairsBench(name)
     else:
         raise SystemExit("unknown workload %s" % name)
     if rows_div > 1:
@@ -376,7 +603,7 @@ def make_workload(name, rows_div=1):
             wl.name = w.name
         else:
             wl.cfg = dict(wl.cfg)
-            key = "rows" if isinstance(wl, RsAgBench) else "target_rows"
+            key = "rows" if isinstance(wl, (RsAgBench, WindowOpBench)) else "target_rows"
             wl.cfg[key] = wl.cfg[key] // rows_div
             wl.name += "_rows_div%d" % rows_div
     return wl
@@ -419,26 +646,24 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s: of fallback"
 
 
-def kernel_source_hash():
-    """Hash of every library source file (kernels, launch code, header)."""
+def kernel_source_hash(files):
+    """Hash of the given library source files (kernels, launch code, header)."""
     h = hashlib.sha256()
-    for d in KERNEL_SOURCE_DIRS:
-        for name in sorted(os.listdir(os.path.join(ROOT, d))):
-            path = os.path.join(ROOT, d, name)
-            if os.path.isfile(path) and name.endswith((".cu", ".cuh", ".h")):
-                h.update(name.encode())
-                with open(path, "rb") as f:
-                    h.update(f.read())
+    for rel in files:
+        h.update(rel.encode())
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name):
+def recorded_traffic(workload_name, files):
     """DRAM bytes per launch recorded from an ncu capture of the current
-    kernel sources (profiles/traffic.txt lines: workload sha bytes), else None."""
+    sources of the workload's kernel (profiles/traffic.txt lines: workload
+    sha bytes), else None."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    sha = kernel_source_hash()
+    sha = kernel_source_hash(files)
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload_name and parts[1] == sha:
@@ -559,6 +784,7 @@ def run_ours(args):
     nl = wl.launches_per_step()
 
     for _ in range(args.warmup):
+        wl.prepare()
         flush(1)
         for i in range(nl):
             wl.launch(i)
@@ -573,6 +799,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
+        wl.prepare()
         flush(k)
         for i in range(nl):
             ev[k][i][0].record(stream)
@@ -594,7 +821,7 @@ def run_ours(args):
         statistics.mean(v for x in per_launch for v in x)
     achieved = wl.bytes_per_launch() / (avg0 / 1e3) / 1e9
     peak, peak_src = measured_peak()
-    traffic = recorded_traffic(wl.name)
+    traffic = recorded_traffic(wl.name, wl.sources)
 
     # end to end: pinned host inputs in, results out, every step
     if args.no_e2e:
@@ -688,7 +915,7 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="treduce",
                     choices=["treduce", "treduce_bf16", "treduce_small", "treduce_f32", "treduce_i32",
-                             "rs_ag", "a2av"])
+                             "rs_ag", "a2av", "allreduce", "broadcast", "all_to_all", "combine"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
