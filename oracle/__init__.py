@@ -70,9 +70,10 @@ def lib():
         L.oracle_all_to_all.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i64, i64, i32]
         L.oracle_all_to_all_v_combine.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
                                                   ctypes.POINTER(vp), i32, i64, i64, i32, i32]
+        L.oracle_credit_barrier.argtypes = [i32, i32, vp, vp, vp, i32]
         for name in ("oracle_treduce", "oracle_reduce_scatter", "oracle_allgather",
                      "oracle_all_to_all_v", "oracle_allreduce", "oracle_broadcast",
-                     "oracle_all_to_all", "oracle_all_to_all_v_combine"):
+                     "oracle_all_to_all", "oracle_all_to_all_v_combine", "oracle_credit_barrier"):
             getattr(L, name).restype = ctypes.c_int
         L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
         L.oracle_f32_to_bf16.restype = ctypes.c_uint16
@@ -139,6 +140,18 @@ def all_to_all_v_combine(windows, outputs, recv_counts, target_rows, size, atomi
     assert len(outputs) == n and len(recv_counts) == n
     return lib().oracle_all_to_all_v_combine(_ptrs(windows), _ptrs(outputs), _ptrs(recv_counts), n,
                                              target_rows, size, atomic, dtype)
+
+
+def credit_barrier(nranks, generations, present, signal, wait_eq=False):
+    """Runs the credit barrier on `signal` (int32 [N, N], row r = rank r's
+    window) in place; returns the per-rank status array."""
+    present = np.ascontiguousarray(present, dtype=np.int32)
+    assert signal.dtype == np.int32 and signal.shape == (nranks, nranks) and signal.flags.c_contiguous
+    status = np.zeros(nranks, dtype=np.int32)
+    rc = lib().oracle_credit_barrier(nranks, generations, present.ctypes.data, signal.ctypes.data,
+                                     status.ctypes.data, 1 if wait_eq else 0)
+    assert rc == 0
+    return status
 
 
 def f32_to_bf16(x):

@@ -494,3 +494,74 @@ int oracle_all_to_all_v_combine(const void* const* windows, void* const* outputs
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Credit barrier                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The self-clearing credit barrier ([DO] "Barrier-signal protocol"), run by a
+ * deterministic scheduler. Rank r's signal window holds one cell per source
+ * rank: signal[r * N + s]. A call of G generations is, for each rank r:
+ *   for g = 1..G:   notify every peer p != r: signal[p*N + r] += 1   (AtomicAdd)
+ *                   wait until signal[r*N + s] >= g for every s != r (Ge)
+ *   epilogue:       signal[r*N + s] -= G for every s != r            (AtomicAdd)
+ * present[r] = 0 models a rank that never arrives. The scheduler visits the
+ * present ranks in ascending order, letting each run until it blocks, and
+ * repeats until a full pass makes no progress; ranks still blocked then time
+ * out. status[r]: 0 = completed, g = timed out waiting in generation g,
+ * -1 = not present. `wait_eq` = 1 replaces the Ge comparison by Eq (the page
+ * explains why that can hang); it exists to demonstrate that point.
+ * The final signal is written back in place.
+ */
+int oracle_credit_barrier(int nranks, int generations, const int32_t* present, int32_t* signal,
+                          int32_t* status, int wait_eq)
+{
+    if (nranks <= 0 || generations < 0) return ORC_BAD_ARG;
+    int N = nranks;
+    int* gen = (int*)calloc((size_t)N, sizeof(int));       /* current generation, 1-based */
+    int* notified = (int*)calloc((size_t)N, sizeof(int));  /* notified in `gen` already */
+    int* done = (int*)calloc((size_t)N, sizeof(int));
+    for (int r = 0; r < N; ++r) {
+        gen[r] = 1;
+        status[r] = present[r] ? 0 : -1;
+        done[r] = present[r] ? 0 : 1;
+    }
+    int progress = 1;
+    while (progress) {
+        progress = 0;
+        for (int r = 0; r < N; ++r) {
+            while (!done[r]) {
+                if (gen[r] > generations) {                 /* epilogue */
+                    for (int s = 0; s < N; ++s)
+                        if (s != r) signal[r * N + s] -= generations;
+                    done[r] = 1;
+                    progress = 1;
+                    break;
+                }
+                if (!notified[r]) {
+                    for (int p = 0; p < N; ++p)
+                        if (p != r) signal[p * N + r] += 1;
+                    notified[r] = 1;
+                    progress = 1;
+                }
+                int ready = 1;
+                for (int s = 0; s < N; ++s) {
+                    if (s == r) continue;
+                    int v = signal[r * N + s];
+                    if (wait_eq ? (v != gen[r]) : (v < gen[r])) ready = 0;
+                }
+                if (!ready) break;                          /* blocked: next rank */
+                gen[r] += 1;
+                notified[r] = 0;
+                progress = 1;
+            }
+        }
+    }
+    for (int r = 0; r < N; ++r)
+        if (!done[r]) status[r] = gen[r];                   /* timed out in this generation */
+    free(gen);
+    free(notified);
+    free(done);
+    return ORC_OK;
+}
