@@ -55,10 +55,11 @@ class L2Flush:
         import torch
         self.a.fill_(k & 0xFF)
         torch.amax(self.b, dim=0, out=self.sink)
-# The sources each workload's dominant kernel is built and launched from: a
-# recorded ncu traffic figure stays valid while these hash the same.
+# The device-code sources of each workload's dominant kernel: a recorded ncu
+# traffic figure stays valid while these hash the same (a change of launch
+# configuration in ptoc_api.cu calls for a new capture too).
 _CSRC = "tile_level_collective_gb300/csrc/"
-_COMMON = [_CSRC + "ptoc_api.cu", _CSRC + "ptoc_internal.h", _CSRC + "reduce_impl.cuh", "include/ptoc.h"]
+_COMMON = [_CSRC + "ptoc_internal.h", _CSRC + "reduce_impl.cuh"]
 REDUCE_SOURCES = _COMMON + [_CSRC + f for f in ("reduce_async.cuh", "reduce_f32.cu", "reduce_f16.cu",
                                                 "reduce_bf16.cu", "reduce_i32.cu")]
 MOVE_SOURCES = _COMMON + [_CSRC + "movement.cu"]
@@ -572,6 +573,45 @@ class PairsBench(A2avBench):
         return 6 * size * moved, dt, "the kAdd combine with capacity %d rows per pair (counts scaled)" % mr
 
 
+class BarrierBench(Workload):
+    """The credit barrier among N ranks simulated on the GPU: one launch of G
+    generations; the metric is the latency of one generation."""
+    metric = "credit barrier latency per generation"
+    unit = "us"
+
+    def __init__(self, nranks=8, generations=1000):
+        self.n, self.g = nranks, generations
+        self.name = "credit_barrier_n%d_g%d" % (nranks, generations)
+        self.kernel = "credit_barrier_kernel (cooperative, one warp per rank)"
+        self.dtype_compute = "i32"
+        self.sources = MOVE_SOURCES
+
+    def launches_per_step(self):
+        return 1
+
+    def bytes_per_step(self):
+        return 0
+
+    def bytes_per_launch(self):
+        return 0
+
+    def setup_host(self):
+        pass
+
+    def setup_device(self, dev):
+        import torch
+        self.sig = [torch.zeros(self.n, dtype=torch.int32, device=dev) for _ in range(self.n)]
+        self.status = torch.zeros(self.n, dtype=torch.int32, device=dev)
+
+    def launch(self, i, srcs=None, dst=None):
+        import tile_level_collective_gb300 as P
+        P.ptoc_credit_barrier(self.sig, list(range(self.n)), self.g, 10 ** 9, self.status)
+
+    def config(self):
+        return {"workload": self.name, "op": "credit barrier", "nranks": self.n, "generations": self.g,
+                "step": "one call of %d generations, all ranks in one cooperative launch" % self.g}
+
+
 def make_workload(name, rows_div=1):
     """The named workload; rows_div > 1 divides its row counts (a smaller case
     of the same kernel, for profiler captures)."""
@@ -593,6 +633,8 @@ def make_workload(name, rows_div=1):
         wl = WindowOpBench(name)
     elif name in ("all_to_all", "combine"):
         wl = PairsBench(name)
+    elif name == "barrier":
+        wl = BarrierBench()
     else:
         raise SystemExit("unknown workload %s" % name)
     if rows_div > 1:
@@ -823,6 +865,17 @@ def run_ours(args):
     peak, peak_src = measured_peak()
     traffic = recorded_traffic(wl.name, wl.sources)
 
+    if isinstance(wl, BarrierBench):
+        if rank == 0:
+            us = ms * 1e3 / wl.g
+            print(json.dumps({"metric": wl.metric, "value": round(us, 4), "unit": wl.unit, "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+                              "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                              "dtype": "i32", "data": "synthetic", "config": wl.config(),
+                              "roofline": None, "e2e": None, "gpu_launches": args.steps,
+                              "clocks": sampler.summary(t0, t1) if sampler else None}), flush=True)
+        return
+
     # end to end: pinned host inputs in, results out, every step
     if args.no_e2e:
         e_ms, e_value = None, None
@@ -882,6 +935,10 @@ def run_reference(args):
     if rank != 0:
         return
     wl = make_workload(args.workload, args.rows_div)
+    if isinstance(wl, BarrierBench):
+        print(json.dumps({"impl": "reference", "unavailable": "the credit barrier has no CPU timing arm "
+                          "(the oracle is a sequential step machine, not a barrier)"}), flush=True)
+        return
     wl.setup_host()
     total_steps = args.steps + args.warmup
     per_step = max(0.002, args.reference_seconds / max(1, total_steps))
@@ -915,7 +972,7 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="treduce",
                     choices=["treduce", "treduce_bf16", "treduce_small", "treduce_f32", "treduce_i32",
-                             "rs_ag", "a2av", "allreduce", "broadcast", "all_to_all", "combine"])
+                             "rs_ag", "a2av", "allreduce", "broadcast", "all_to_all", "combine", "barrier"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)

@@ -9,8 +9,9 @@
  *   [TR] "CANN PTO-ISA TREDUCE 指令详解" (TREDUCE instruction explained,
  *        lpnh.cn news 2291107), sections 1-8.
  *   [DO] "Distributed Operators (N6)" (pypto.ai dev/distributed_ops): the op
- *        table in "Overview", "ABI enums", "pld.tensor.all_to_all_v",
- *        "pld.tensor.allreduce", "pld.tensor.put", "pld.tile.remote_store".
+ *        table in "Overview", "ABI enums", "Barrier-signal protocol",
+ *        "pld.tensor.all_to_all_v", "pld.tensor.allreduce", "pld.tensor.put",
+ *        "pld.tile.remote_store".
  *
  * Conventions shared by every entry point
  *   - Every data pointer is a DEVICE pointer on the calling thread's current
@@ -234,6 +235,39 @@ ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, const ptoc_grou
                                       const int32_t* const* recv_counts,
                                       int64_t target_rows, int64_t size, ptoc_atomic_type atomic,
                                       ptoc_dtype dtype, cudaStream_t stream);
+
+/*
+ * ptoc_credit_barrier - the self-clearing credit barrier ([DO]
+ * "Barrier-signal protocol") among ranks simulated on this GPU.
+ *   signals->tensors[p] : rank p's signal window, N device int32 cells; cell s
+ *                         counts the credits rank s has given rank p. All
+ *                         cells must be zero when a call starts (they are
+ *                         zero again after every complete call).
+ *   local_ranks         : host array of the n_local distinct ranks that take
+ *                         part in this launch (1 <= n_local <= N).
+ *   status              : device int32[n_local]; status[i] = 0 if
+ *                         local_ranks[i] completed, or g if it gave up
+ *                         waiting in generation g.
+ * For g = 1..generations every rank adds 1 (atomic, release) to its cell in
+ * every peer's window and waits (acquire) until every cell of its own window
+ * is >= g (Ge, not Eq: a fast peer may already be ahead); then it subtracts
+ * `generations` from its own cells. All local ranks run in one cooperative
+ * launch (one warp each). A rank that is not local never arrives, so the
+ * others give up after timeout_ns nanoseconds (0 < timeout_ns <= 60 s) and
+ * skip their epilogue, leaving credits in the windows, as the page describes
+ * for an aborted call: clear them with ptoc_signal_reset before reuse.
+ * Errors: invalid arguments, overlapping windows or status
+ * (PTOC_ERR_ALIAS), no cooperative-launch support (PTOC_ERR_UNSUPPORTED).
+ */
+ptoc_status ptoc_credit_barrier(const ptoc_group* signals, const int32_t* local_ranks, int32_t n_local,
+                                int32_t generations, int64_t timeout_ns, int32_t* status,
+                                cudaStream_t stream);
+
+/*
+ * ptoc_signal_reset - zero every cell of every signal window on `stream`
+ * (the host-side reset the page prescribes after an aborted call).
+ */
+ptoc_status ptoc_signal_reset(const ptoc_group* signals, cudaStream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char* ptoc_status_string(ptoc_status status);

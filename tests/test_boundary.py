@@ -25,7 +25,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert declared_functions() == ["ptoc_all_to_all", "ptoc_all_to_all_v", "ptoc_all_to_all_v_combine",
                                     "ptoc_allgather", "ptoc_allreduce", "ptoc_broadcast",
-                                    "ptoc_reduce_scatter", "ptoc_status_string", "ptoc_treduce"]
+                                    "ptoc_credit_barrier", "ptoc_reduce_scatter", "ptoc_signal_reset",
+                                    "ptoc_status_string", "ptoc_treduce"]
 
 
 def test_library_exports_every_declared_symbol():
@@ -161,3 +162,21 @@ def test_all_to_all_and_combine_reject():
     assert C(ins, tgs, [rc[0] + 2] + rc[1:], 64, 16, P.ATOMIC_NONE, P.BF16, stream=0,
              check=False) == P.ERR_INVALID_ARG                                             # misaligned counts
     assert C(ins, tgs, rc, 3, 16, P.ATOMIC_ADD, P.BF16, stream=0, check=False) == P.OK     # MAX_RECV 0
+
+
+def test_credit_barrier_rejects():
+    sig = [A + 512 * r for r in range(4)]
+    ST = A + 64 * MB
+    B = P.ptoc_credit_barrier
+    assert B(sig, [], 1, 10 ** 9, ST, stream=0, check=False) == P.ERR_INVALID_ARG         # no local rank
+    assert B(sig, [0, 4], 1, 10 ** 9, ST, stream=0, check=False) == P.ERR_INVALID_ARG     # rank out of range
+    assert B(sig, [1, 1], 1, 10 ** 9, ST, stream=0, check=False) == P.ERR_INVALID_ARG     # duplicate
+    assert B(sig, [0], -1, 10 ** 9, ST, stream=0, check=False) == P.ERR_INVALID_ARG       # generations
+    assert B(sig, [0], 1, 0, ST, stream=0, check=False) == P.ERR_INVALID_ARG              # timeout
+    assert B(sig, [0], 1, 61 * 10 ** 9, ST, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert B(sig, [0], 1, 10 ** 9, 0, stream=0, check=False) == P.ERR_INVALID_ARG         # status
+    assert B(sig, [0], 1, 10 ** 9, ST + 2, stream=0, check=False) == P.ERR_INVALID_ARG
+    assert B([A, A + 8, A + 1024, A + 2048], [0], 1, 10 ** 9, ST, stream=0, check=False) == P.ERR_ALIAS
+    assert B(sig, [0, 1], 1, 10 ** 9, sig[2] + 4, stream=0, check=False) == P.ERR_ALIAS  # status over a window
+    assert P.ptoc_signal_reset([A, 0], stream=0, check=False) == P.ERR_INVALID_ARG
+    assert P.ptoc_signal_reset([A + 2], stream=0, check=False) == P.ERR_INVALID_ARG

@@ -18,6 +18,9 @@ Entry points carry the C names:
     ptoc_all_to_all(inputs, targets, target_rows, size, dtype, stream=None)
     ptoc_all_to_all_v_combine(windows, outputs, recv_counts, target_rows, size,
                               atomic, dtype, stream=None)
+    ptoc_credit_barrier(signals, local_ranks, generations, timeout_ns, status,
+                        stream=None)
+    ptoc_signal_reset(signals, stream=None)
 
 Buffers are torch tensors or raw device addresses (ints). ``stream=None``
 means torch's current stream. A non-OK status raises :class:`PtocError`
@@ -69,8 +72,12 @@ _lib.ptoc_broadcast.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, _vp]
 _lib.ptoc_all_to_all.argtypes = [_G, _G, _i64, _i64, ctypes.c_int, _vp]
 _lib.ptoc_all_to_all_v_combine.argtypes = [_G, _G, ctypes.POINTER(_vp), _i64, _i64, ctypes.c_int,
                                            ctypes.c_int, _vp]
+_lib.ptoc_credit_barrier.argtypes = [_G, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
+                                     _i64, _vp, _vp]
+_lib.ptoc_signal_reset.argtypes = [_G, _vp]
 for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v",
-           "ptoc_allreduce", "ptoc_broadcast", "ptoc_all_to_all", "ptoc_all_to_all_v_combine"):
+           "ptoc_allreduce", "ptoc_broadcast", "ptoc_all_to_all", "ptoc_all_to_all_v_combine",
+           "ptoc_credit_barrier", "ptoc_signal_reset"):
     getattr(_lib, _f).restype = ctypes.c_int
 _lib.ptoc_status_string.argtypes = [ctypes.c_int]
 _lib.ptoc_status_string.restype = ctypes.c_char_p
@@ -180,6 +187,20 @@ def ptoc_all_to_all_v_combine(windows, outputs, recv_counts, target_rows, size, 
     st = _lib.ptoc_all_to_all_v_combine(ctypes.byref(gw), ctypes.byref(go), rc, target_rows, size,
                                         int(atomic), int(dtype), _stream(stream))
     return _done(st, "ptoc_all_to_all_v_combine", check)
+
+
+def ptoc_credit_barrier(signals, local_ranks, generations, timeout_ns, status, stream=None, check=True):
+    g, keep = _group(signals)
+    ranks = (ctypes.c_int32 * max(len(local_ranks), 1))(*[int(r) for r in local_ranks])
+    st = _lib.ptoc_credit_barrier(ctypes.byref(g), ranks, len(local_ranks), int(generations),
+                                  int(timeout_ns), _addr(status), _stream(stream))
+    return _done(st, "ptoc_credit_barrier", check)
+
+
+def ptoc_signal_reset(signals, stream=None, check=True):
+    g, keep = _group(signals)
+    st = _lib.ptoc_signal_reset(ctypes.byref(g), _stream(stream))
+    return _done(st, "ptoc_signal_reset", check)
 
 
 # ---- shape-inferring conveniences over torch tensors ------------------------

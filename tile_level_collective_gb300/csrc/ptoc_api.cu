@@ -603,6 +603,59 @@ extern "C" ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, cons
     return launch_pairs(p, windows->tensors, outputs->tensors, n, eb, dtype, atomic == PTOC_ATOMIC_ADD, stream);
 }
 
+extern "C" ptoc_status ptoc_credit_barrier(const ptoc_group* signals, const int32_t* local_ranks, int32_t n_local,
+                                           int32_t generations, int64_t timeout_ns, int32_t* status,
+                                           cudaStream_t stream)
+{
+    ptoc_status st = check_group(signals, false);
+    if (st != PTOC_OK) return st;
+    const int n = signals->nranks;
+    if (!local_ranks || !status) return PTOC_ERR_INVALID_ARG;
+    if (n_local < 1 || n_local > n) return PTOC_ERR_INVALID_ARG;
+    if (generations < 0 || generations > (1 << 30)) return PTOC_ERR_INVALID_ARG;
+    if (timeout_ns <= 0 || timeout_ns > (int64_t)60 * 1000 * 1000 * 1000) return PTOC_ERR_INVALID_ARG;
+    if (!aligned(status, 4)) return PTOC_ERR_INVALID_ARG;
+    bool seen[kMaxRanks] = {false};
+    for (int i = 0; i < n_local; ++i) {
+        const int r = local_ranks[i];
+        if (r < 0 || r >= n || seen[r]) return PTOC_ERR_INVALID_ARG;
+        seen[r] = true;
+    }
+    for (int r = 0; r < n; ++r)
+        if (!aligned(signals->tensors[r], 4)) return PTOC_ERR_INVALID_ARG;
+    Span writes[kMaxRanks + 1];
+    for (int r = 0; r < n; ++r) writes[r] = Span{signals->tensors[r], (uintptr_t)n * 4u};
+    writes[n] = Span{status, (uintptr_t)n_local * 4u};
+    st = check_disjoint_outputs(writes, n + 1, nullptr, 0);
+    if (st != PTOC_OK) return st;
+
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, current_device()) != cudaSuccess || !coop)
+        return PTOC_ERR_UNSUPPORTED;
+    BarrierParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r) p.sig[r] = (int32_t*)signals->tensors[r];
+    for (int i = 0; i < n_local; ++i) p.local[i] = local_ranks[i];
+    p.status = status;
+    p.timeout_ns = timeout_ns;
+    p.nranks = n;
+    p.nlocal = n_local;
+    p.generations = generations;
+    return launch_credit_barrier(p, stream) == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+}
+
+extern "C" ptoc_status ptoc_signal_reset(const ptoc_group* signals, cudaStream_t stream)
+{
+    ptoc_status st = check_group(signals, false);
+    if (st != PTOC_OK) return st;
+    const int n = signals->nranks;
+    for (int r = 0; r < n; ++r)
+        if (!aligned(signals->tensors[r], 4)) return PTOC_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r)
+        if (cudaMemsetAsync(signals->tensors[r], 0, (size_t)n * 4u, stream) != cudaSuccess) return PTOC_ERR_CUDA;
+    return PTOC_OK;
+}
+
 extern "C" const char* ptoc_status_string(ptoc_status s)
 {
     switch (s) {

@@ -80,6 +80,20 @@ struct A2avParams {
     int32_t publish;              // 1: write pub[b][a]
 };
 
+// The credit barrier: sig[p] is rank p's signal window (nranks int32 cells,
+// cell s = credits from rank s); the launch runs the ranks local[0..nlocal),
+// one warp each; status[i] receives local[i]'s result (0, or the generation it
+// timed out in).
+struct BarrierParams {
+    int32_t* sig[kMaxRanks];
+    int32_t local[kMaxRanks];
+    int32_t* status;
+    int64_t timeout_ns;
+    int32_t nranks, nlocal, generations;
+};
+
+cudaError_t launch_credit_barrier(const BarrierParams& p, cudaStream_t s);
+
 // Launchers (one translation unit per element type for the reductions).
 // `vb` is the vector width in bytes (16, 8 or 4; 2 for 16-bit data that is
 // only 2-byte aligned). They return the launch status; they never allocate.
