@@ -9,8 +9,8 @@ Min (three launches). Metric: effective HBM GB/s = (N + 1) * bytes/elem *
 valid elements per launch, summed over the step, divided by the step's device
 time. Inputs are generated on the host by the seeded generator and resident in
 HBM before timing; before every step L2 is flushed outside the timed events
-(a 256 MiB write, then a 256 MiB read of another buffer, so that no dirty
-flush lines are left for the timed kernels to write back). Other workloads
+(a 256 MiB buffer is written, then read back, which leaves L2 cold and clean:
+no dirty flush lines for the timed kernels to write back). Other workloads
 (the parity configurations) can be timed with --workload for the per-kernel
 evidence.
 
@@ -37,24 +37,27 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 
 
-L2_NOTE = ("flushed before every step, outside the timed events: 256 MiB write, then 256 MiB read "
-           "of another buffer (cold, clean L2)")
+L2_NOTE = ("flushed before every step, outside the timed events: a 256 MiB buffer is written, then "
+           "read back (cold, clean L2)")
 
 
 class L2Flush:
-    """Leaves L2 cold and clean: writes one buffer larger than L2, then reads
-    another one, which evicts (writes back) the dirty lines of the first."""
+    """Leaves L2 cold and clean: writes a buffer twice the size of L2, then
+    reads the same buffer back. Measured on GB300: a write alone leaves dirty
+    lines that the next kernel must write back, and a read of another buffer
+    does not clear them either; reading the written buffer back does, and the
+    kernels that follow then take their ncu cold-cache durations."""
 
     def __init__(self, dev):
         import torch
         self.a = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        self.b = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.words = self.a.view(torch.int32)
         self.sink = torch.empty((), dtype=torch.int32, device=dev)
 
     def __call__(self, k=0):
         import torch
         self.a.fill_(k & 0xFF)
-        torch.amax(self.b, dim=0, out=self.sink)
+        torch.amax(self.words, dim=0, out=self.sink)
 # The device-code sources of each workload's dominant kernel: a recorded ncu
 # traffic figure stays valid while these hash the same (a change of launch
 # configuration in ptoc_api.cu calls for a new capture too).
