@@ -35,60 +35,71 @@ NUMPY_TYPE = {F32: np.float32, F16: np.uint16, BF16: np.uint16, I32: np.int32}
 _lib = None
 
 
+def compile_source(src, out):
+    """gcc with the oracle's flags: src (C file) -> out (shared library)."""
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(os.path.abspath(out)))
+    os.close(fd)
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    try:
+        subprocess.check_call(cmd)
+        os.replace(tmp, out)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return out
+
+
 def build(force=False):
     """Compile oracle.c into liboracle.so beside it (gcc, plain flags)."""
     if (not force and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
-    os.close(fd)
-    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
-    try:
-        subprocess.check_call(cmd)
-        os.replace(tmp, _LIB)
-    finally:
-        if os.path.exists(tmp):
-            os.unlink(tmp)
-    return _LIB
+    return compile_source(_SRC, _LIB)
 
 
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB)
-        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        L.oracle_treduce.argtypes = [ctypes.POINTER(vp), i32, i32, vp, i64, i64, i64, i32, i32]
-        L.oracle_reduce_scatter.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
-        L.oracle_allgather.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32]
-        L.oracle_all_to_all_v.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
-                                          ctypes.POINTER(vp), ctypes.POINTER(vp),
-                                          i32, i64, i64, i32]
-        L.oracle_allreduce.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
-        L.oracle_broadcast.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i64, i64, i32]
-        L.oracle_all_to_all.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i64, i64, i32]
-        L.oracle_all_to_all_v_combine.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
-                                                  ctypes.POINTER(vp), i32, i64, i64, i32, i32]
-        L.oracle_credit_barrier.argtypes = [i32, i32, vp, vp, vp, i32]
-        for name in ("oracle_treduce", "oracle_reduce_scatter", "oracle_allgather",
-                     "oracle_all_to_all_v", "oracle_allreduce", "oracle_broadcast",
-                     "oracle_all_to_all", "oracle_all_to_all_v_combine", "oracle_credit_barrier"):
-            getattr(L, name).restype = ctypes.c_int
-        L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
-        L.oracle_f32_to_bf16.restype = ctypes.c_uint16
-        L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
-        L.oracle_f32_to_f16.restype = ctypes.c_uint16
-        L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
-        L.oracle_bf16_to_f32.restype = ctypes.c_float
-        L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
-        L.oracle_f16_to_f32.restype = ctypes.c_float
-        for name in ("oracle_f32_to_bf16_array", "oracle_f32_to_f16_array",
-                     "oracle_f16_to_f32_array", "oracle_bf16_to_f32_array"):
-            getattr(L, name).argtypes = [vp, vp, i64]
-            getattr(L, name).restype = None
-        _lib = L
+        _lib = load(_LIB)
     return _lib
+
+
+def load(path):
+    """Load an oracle build and declare its functions (the tests also load
+    deliberately broken copies, to show that the pins catch them)."""
+    L = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.oracle_treduce.argtypes = [ctypes.POINTER(vp), i32, i32, vp, i64, i64, i64, i32, i32]
+    L.oracle_reduce_scatter.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
+    L.oracle_allgather.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32]
+    L.oracle_all_to_all_v.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                      ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                      i32, i64, i64, i32]
+    L.oracle_allreduce.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
+    L.oracle_broadcast.argtypes = [ctypes.POINTER(vp), i32, i32, i64, i64, i64, i32]
+    L.oracle_all_to_all.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i64, i64, i32]
+    L.oracle_all_to_all_v_combine.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                              ctypes.POINTER(vp), i32, i64, i64, i32, i32]
+    L.oracle_credit_barrier.argtypes = [i32, i32, vp, vp, vp, i32]
+    for name in ("oracle_treduce", "oracle_reduce_scatter", "oracle_allgather",
+                 "oracle_all_to_all_v", "oracle_allreduce", "oracle_broadcast",
+                 "oracle_all_to_all", "oracle_all_to_all_v_combine", "oracle_credit_barrier"):
+        getattr(L, name).restype = ctypes.c_int
+    L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_f16.restype = ctypes.c_uint16
+    L.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_f32.restype = ctypes.c_float
+    L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+    L.oracle_f16_to_f32.restype = ctypes.c_float
+    for name in ("oracle_f32_to_bf16_array", "oracle_f32_to_f16_array",
+                 "oracle_f16_to_f32_array", "oracle_bf16_to_f32_array"):
+        getattr(L, name).argtypes = [vp, vp, i64]
+        getattr(L, name).restype = None
+    return L
 
 
 def _ptrs(arrays):

@@ -190,3 +190,14 @@ def test_dispatch_then_combine_round_trip(orc, dtype, n, tr, size):
         got, orig = dec(outs[s], dtype), dec(inputs[s], dtype)
         np.testing.assert_array_equal(got[sent[s]], 2 * orig[sent[s]])
         np.testing.assert_array_equal(got[~sent[s]], orig[~sent[s]])
+
+
+def test_allreduce_order_golden(orc):
+    """Every window gets the reduction in rank order 0..N-1, whatever its own
+    rank: with ranks holding (1, 1, 2^24) that is 1 + 1 + 2^24 = 2^24 + 2 on
+    every window (a rank-first order would give 2^24 on window 2)."""
+    g = golden("treduce_rank_order_f32.json")
+    want = next(c["expected_sum"] for c in g["cases"] if c["root"] == 0)
+    wins = [np.array([[v]], np.float32) for v in g["values"]]
+    assert orc.allreduce(wins, 1, 1, 1, OPS["sum"], DT["f32"]) == 0
+    assert all(w[0, 0] == np.float32(want) for w in wins)
