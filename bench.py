@@ -75,6 +75,10 @@ MOVE_SOURCES = _COMMON + [_CSRC + "movement.cu"]
 class Workload:
     """One benchmark workload: host inputs, device buffers, the launches of a
     step and its algorithmic bytes."""
+    # Launches of different kernels in one step are timed one by one (events
+    # between them); launches of one kernel family are timed as a step (events
+    # around it), so they run back to back as a caller's calls do.
+    per_launch_timing = False
     name = ""
     dtype_compute = "f32"
     storage = ""
@@ -187,6 +191,7 @@ class RsAgBench(Workload):
         import synth
         self.cfg = synth.CONFIG4
         self.name = "reduce_scatter_allgather_n8_f16_8192x4096"
+        self.per_launch_timing = True
         self.storage = "f16"
         self.kernel = "reduce_async_kernel<f16> (scatter mode) + gather_kernel"
 
@@ -838,7 +843,8 @@ def run_ours(args):
     sampler = ClockSampler(local) if not args.no_clocks else None
     if sampler:
         time.sleep(0.6)          # let the sampler start before the timed region
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nl)]
+    nev = nl if wl.per_launch_timing else 1
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nev)]
           for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
@@ -846,24 +852,33 @@ def run_ours(args):
     for k in range(args.steps):
         wl.prepare()
         flush(k)
-        for i in range(nl):
-            ev[k][i][0].record(stream)
-            wl.launch(i)
-            ev[k][i][1].record(stream)
+        if wl.per_launch_timing:
+            for i in range(nl):
+                ev[k][i][0].record(stream)
+                wl.launch(i)
+                ev[k][i][1].record(stream)
+        else:
+            ev[k][0][0].record(stream)
+            for i in range(nl):
+                wl.launch(i)
+            ev[k][0][1].record(stream)
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
     if sampler:
         sampler.stop()
-    per_launch = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(nl)] for k in range(args.steps)]
-    # a step = its launches back to back on the stream (the flush between steps excluded)
-    step_ms = [sum(x) for x in per_launch]
+    timed = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(nev)] for k in range(args.steps)]
+    # a step = its launches on the stream (the flush between steps excluded)
+    step_ms = [sum(x) for x in timed]
     ms_local = sum(step_ms) / args.steps
     ms, value = aggregate(ms_local, wl.bytes_per_step(), world, dev)
 
-    # roofline of the dominant kernel: launch 0's family
-    avg0 = statistics.mean(x[0] for x in per_launch) if nl == 1 or args.workload == "rs_ag" else \
-        statistics.mean(v for x in per_launch for v in x)
+    # roofline of the dominant kernel: launch 0 when launches are timed one by
+    # one, else the step's average launch (all of one kernel family)
+    if wl.per_launch_timing:
+        avg0 = statistics.mean(x[0] for x in timed)
+    else:
+        avg0 = statistics.mean(step_ms) / nl
     achieved = wl.bytes_per_launch() / (avg0 / 1e3) / 1e9
     peak, peak_src = measured_peak()
     traffic = recorded_traffic(wl.name, wl.sources)
@@ -927,6 +942,9 @@ def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traff
             "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": round(e_ms, 6),
             "path": "pinned host -> device copy, the library calls, device -> pinned host copy"},
         "gpu_launches": nl * args.steps,
+        "timing": ("CUDA events around each launch" if wl.per_launch_timing else
+                   "CUDA events around each step; its %d launches run back to back (programmatic "
+                   "dependent launch lets each overlap the previous one's tail)" % nl),
         "clocks": clocks,
     }
     return line

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kBlock) gather_kernel(const __grid_constant__ 
     using C = Chunk<VB>;
     constexpr int VE = VB / EB;
     const int n = p.nranks;
+    pdl_enter();
     for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
         const int64_t row = t / p.tpr;
         const int64_t seg = t - row * p.tpr;
@@ -74,12 +75,11 @@ __global__ void __launch_bounds__(kBlock) gather_kernel(const __grid_constant__ 
 template <int EB>
 static cudaError_t launch_gather_eb(const GatherParams& p, int vb, dim3 grid, cudaStream_t s)
 {
-    if (vb == 16) gather_kernel<EB, 16><<<grid, kBlock, 0, s>>>(p);
-    else if (vb == 8) gather_kernel<EB, 8><<<grid, kBlock, 0, s>>>(p);
-    else if (vb == 4) gather_kernel<EB, 4><<<grid, kBlock, 0, s>>>(p);
-    else if constexpr (EB == 2) gather_kernel<2, 2><<<grid, kBlock, 0, s>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (vb == 16) return launch_kernel(gather_kernel<EB, 16>, grid, kBlock, 0, s, p);
+    if (vb == 8) return launch_kernel(gather_kernel<EB, 8>, grid, kBlock, 0, s, p);
+    if (vb == 4) return launch_kernel(gather_kernel<EB, 4>, grid, kBlock, 0, s, p);
+    if constexpr (EB == 2) return launch_kernel(gather_kernel<2, 2>, grid, kBlock, 0, s, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s)
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kBlock) pairs_kernel(const __grid_constant__ A
     const int np = n * n;
     int32_t* cnt = smem;                    // np entries
     int32_t* pre = smem + np;               // np + 1 entries
+    pdl_enter();
     build_pairs(p, cnt, pre, warp_tot);
     const int32_t total = pre[np];
 
@@ -238,11 +239,10 @@ template <int U>
 static cudaError_t launch_a2av_u(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
     const size_t smem = a2av_smem_bytes(p.nranks);
-    if (vb == 16) pairs_kernel<CopyMover<16>, 16, U><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 8) pairs_kernel<CopyMover<8>, 8, U><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 4) pairs_kernel<CopyMover<4>, 4, U><<<grid, kBlock, smem, s>>>(p);
-    else pairs_kernel<CopyMover<2>, 2, U><<<grid, kBlock, smem, s>>>(p);
-    return cudaGetLastError();
+    if (vb == 16) return launch_kernel(pairs_kernel<CopyMover<16>, 16, U>, grid, kBlock, smem, s, p);
+    if (vb == 8) return launch_kernel(pairs_kernel<CopyMover<8>, 8, U>, grid, kBlock, smem, s, p);
+    if (vb == 4) return launch_kernel(pairs_kernel<CopyMover<4>, 4, U>, grid, kBlock, smem, s, p);
+    return launch_kernel(pairs_kernel<CopyMover<2>, 2, U>, grid, kBlock, smem, s, p);
 }
 
 cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s)
@@ -281,12 +281,12 @@ template <class T>
 static cudaError_t launch_add_t(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
     const size_t smem = a2av_smem_bytes(p.nranks);
-    if (vb == 16) pairs_kernel<AddMover<T, 16>, 16, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 8) pairs_kernel<AddMover<T, 8>, 8, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
-    else if (vb == 4) pairs_kernel<AddMover<T, 4>, 4, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
-    else if constexpr (sizeof(T) == 2) pairs_kernel<AddMover1<T>, 2, kAddUnroll><<<grid, kBlock, smem, s>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (vb == 16) return launch_kernel(pairs_kernel<AddMover<T, 16>, 16, kAddUnroll>, grid, kBlock, smem, s, p);
+    if (vb == 8) return launch_kernel(pairs_kernel<AddMover<T, 8>, 8, kAddUnroll>, grid, kBlock, smem, s, p);
+    if (vb == 4) return launch_kernel(pairs_kernel<AddMover<T, 4>, 4, kAddUnroll>, grid, kBlock, smem, s, p);
+    if constexpr (sizeof(T) == 2)
+        return launch_kernel(pairs_kernel<AddMover1<T>, 2, kAddUnroll>, grid, kBlock, smem, s, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, cudaStream_t s)

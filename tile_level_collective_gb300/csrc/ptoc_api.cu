@@ -13,6 +13,13 @@
 #include "ptoc_internal.h"
 
 namespace ptoc {
+
+bool programmatic_launch()
+{
+    const char* e = getenv("PTOC_PDL");
+    return !(e && strcmp(e, "0") == 0);
+}
+
 namespace {
 
 int elem_size(int dtype)

@@ -79,6 +79,7 @@ template <class T, int OP, int S, int G, int B>
 __global__ void __launch_bounds__(B, 512 / B) reduce_async_kernel(const __grid_constant__ ReduceParams p)
 {
     extern __shared__ uint4 stage[];          // [S][G][B] 16-byte slots
+    pdl_enter();
     constexpr int VE = 16 / (int)sizeof(T);
     const int n = p.nranks;
     const int ngroups = (n + G - 1) / G;
@@ -152,8 +153,8 @@ __global__ void __launch_bounds__(B, 512 / B) reduce_async_kernel(const __grid_c
 template <class T, int OP, int C>
 cudaError_t launch_async_cfg(const ReduceParams& p, int grid, cudaStream_t s)
 {
-    reduce_async_kernel<T, OP, kAsyncS[C], kAsyncG[C], kAsyncB[C]><<<grid, kAsyncB[C], async_smem_bytes(C), s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(reduce_async_kernel<T, OP, kAsyncS[C], kAsyncG[C], kAsyncB[C]>, dim3((unsigned)grid),
+                         (unsigned)kAsyncB[C], async_smem_bytes(C), s, p);
 }
 
 // Resident CTAs per SM of one pipelined kernel (sets the shared-memory opt-in

@@ -400,6 +400,40 @@ __device__ __forceinline__ void store_elem(const ReduceParams& p, int64_t row, i
     }
 }
 
+// ---- programmatic dependent launch -----------------------------------------
+
+// Called first by every data kernel: wait until the previous grid in the
+// stream has completed and its writes are visible (a no-op for an ordinary
+// launch), then allow the next programmatic launch to start scheduling.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
+// Launch `kernel` on `s`, as a programmatic dependent launch when enabled:
+// the launch may overlap the tail of the previous kernel of the stream, which
+// pdl_enter then waits for.
+template <class K, class P>
+cudaError_t launch_kernel(K kernel, dim3 grid, unsigned block, size_t smem, cudaStream_t s, const P& p)
+{
+    if (!programmatic_launch()) {
+        kernel<<<grid, block, smem, s>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // ---- the kernel --------------------------------------------------------------
 
 template <class T, int OP, int VB, int U>
@@ -493,6 +527,7 @@ __device__ __forceinline__ void reduce_elements(const ReduceParams& p)
 template <class T, int OP, int VB, int U>
 __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ ReduceParams p)
 {
+    pdl_enter();
     if constexpr (VB < 4) {
         reduce_elements<T, OP, U>(p);
     } else {
@@ -503,9 +538,8 @@ __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ 
 template <class T, int OP, int VB>
 cudaError_t launch_reduce_vb(const ReduceParams& p, int unroll, dim3 grid, cudaStream_t s)
 {
-    if (unroll == 2) reduce_kernel<T, OP, VB, 2><<<grid, kBlock, 0, s>>>(p);
-    else reduce_kernel<T, OP, VB, 1><<<grid, kBlock, 0, s>>>(p);
-    return cudaGetLastError();
+    if (unroll == 2) return launch_kernel(reduce_kernel<T, OP, VB, 2>, grid, kBlock, 0, s, p);
+    return launch_kernel(reduce_kernel<T, OP, VB, 1>, grid, kBlock, 0, s, p);
 }
 
 template <class T, int OP>
