@@ -212,5 +212,8 @@ def test_reduce_scatter_both_kernels(variant, dtype, monkeypatch):
 
 @pytest.mark.parametrize("unroll", ["4", "8"])
 def test_all_to_all_v_both_unrolls(unroll, monkeypatch):
+    """The exchange kernel at both of its unrolls (PTOC_A2AV_UNROLL)."""
     monkeypatch.setenv("PTOC_A2AV_UNROLL", unroll)
     run_a2av(6, 600, 520, np.uint16, -5, 110, seed=33)
+    run_a2av(16, 3200, 1024, np.uint16, -40, 260, seed=34)
+    run_a2av(3, 30, 8, np.float32, -2, 12, seed=35)
