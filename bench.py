@@ -130,21 +130,38 @@ class TreduceBench(Workload):
         P.ptoc_treduce(srcs or self.dev, dst if dst is not None else self.dsts[i], w.rows, w.cols,
                        w.valid_rows, w.valid_cols, w.ld, P.OPS[w.ops[i]], code)
 
-    # e2e: inputs copied from pinned host memory each step, results read back
+    # e2e: every step uploads its inputs from pinned host memory and reads its
+    # results back; double-buffered on three streams, so step k's upload
+    # overlaps step k-1's compute and download (a caller streaming batches).
+    pipelined_e2e = True
+
     def setup_e2e(self, dev):
         import torch
         self.pinned = [_pin(h) for h in self.host]
-        self.out_pinned = [torch.empty(_nbytes(self.dst_init), dtype=torch.uint8).pin_memory()
-                           for _ in self.w.ops]
-        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+        self.e2e_in = [[torch.empty_like(t) for t in self.dev] for _ in range(2)]
+        # fresh destinations (the pad pattern), so the check below sees only
+        # what the pipelined calls wrote
+        self.e2e_out = [[_to_dev(self.dst_init, dev) for _ in self.w.ops] for _ in range(2)]
+        self.out_pinned = [[torch.empty(_nbytes(self.dst_init), dtype=torch.uint8).pin_memory()
+                            for _ in self.w.ops] for _ in range(2)]
 
-    def e2e_step(self):
-        for d, h in zip(self.e2e_dev, self.pinned):
+    def e2e_upload(self, b):
+        for d, h in zip(self.e2e_in[b], self.pinned):
             d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+
+    def e2e_compute(self, b):
         for i in range(self.launches_per_step()):
-            self.launch(i, srcs=self.e2e_dev)
-        for i, o in enumerate(self.out_pinned):
-            o.copy_(self.dsts[i].view(-1).view(torch_uint8()), non_blocking=True)
+            self.launch(i, srcs=self.e2e_in[b], dst=self.e2e_out[b][i])
+
+    def e2e_download(self, b):
+        for o, d in zip(self.out_pinned[b], self.e2e_out[b]):
+            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+
+    def e2e_verify(self, b):
+        """The downloaded results equal the resident run's bytes (same inputs)."""
+        for o, d in zip(self.out_pinned[b], self.dsts):
+            if not bool((o == d.view(-1).view(torch_uint8()).cpu()).all()):
+                raise RuntimeError("pipelined end-to-end result differs from the resident result")
 
     def h2d_bytes(self):
         return sum(_nbytes(h) for h in self.host)
@@ -908,8 +925,59 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_e2e_pipelined(wl, args, dev, world, barrier):
+    """Steps of upload -> compute -> download on three streams with two
+    buffer sets: step k's upload waits for step k-2's compute to release its
+    input set, its compute for its upload and for step k-2's download to
+    release its output set; the timed region spans the first upload to the
+    last download."""
+    import torch
+    wl.setup_e2e(dev)
+    up, comp, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    uploaded, computed, downloaded = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    used = [False, False]
+
+    def run(steps):
+        for k in range(steps):
+            b = k & 1
+            with torch.cuda.stream(up):
+                if used[b]:
+                    up.wait_event(computed[b])
+                wl.e2e_upload(b)
+                uploaded[b].record(up)
+            with torch.cuda.stream(comp):
+                comp.wait_event(uploaded[b])
+                if used[b]:
+                    comp.wait_event(downloaded[b])
+                wl.e2e_compute(b)
+                computed[b].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[b])
+                wl.e2e_download(b)
+                downloaded[b].record(down)
+            used[b] = True
+
+    run(max(2, min(args.warmup, 3)))
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.e2e_steps, args.steps))
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    es.record(up)
+    run(e_steps)
+    down.wait_stream(up)
+    down.wait_stream(comp)
+    ee.record(down)
+    torch.cuda.synchronize()
+    wl.e2e_verify((e_steps - 1) & 1)
+    return aggregate(es.elapsed_time(ee) / e_steps, wl.bytes_per_step(), world, dev)
+
+
 def run_e2e(wl, args, dev, stream, world, barrier):
     import torch
+    if getattr(wl, "pipelined_e2e", False):
+        return run_e2e_pipelined(wl, args, dev, world, barrier)
     wl.setup_e2e(dev)
     for _ in range(max(1, min(args.warmup, 3))):
         wl.e2e_step()
@@ -940,7 +1008,10 @@ def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traff
         "e2e": None if e_value is None else {
             "value": round(e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes(),
             "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": round(e_ms, 6),
-            "path": "pinned host -> device copy, the library calls, device -> pinned host copy"},
+            "path": ("every step: pinned host -> device copy of its inputs, the library calls, device -> "
+                     "pinned host copy of its results" +
+                     ("; double-buffered on three streams (upload of step k overlaps compute and download "
+                      "of step k-1)" if getattr(wl, "pipelined_e2e", False) else ""))},
         "gpu_launches": nl * args.steps,
         "timing": ("CUDA events around each launch" if wl.per_launch_timing else
                    "CUDA events around each step; its %d launches run back to back (programmatic "
