@@ -200,6 +200,33 @@ class TreduceBench(Workload):
         nb, dt, _ = self.oracle_sample(8)
         return 8.0 / max(dt, 1e-9)
 
+    def oracle_sample_threaded(self, rows, threads):
+        """The same oracle call on `rows` rows, the rows split into `threads`
+        contiguous slices run on as many host threads (ctypes releases the
+        interpreter lock during the call)."""
+        import numpy as np
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+        w = self.w
+        rows = max(threads, min(rows, w.valid_rows))
+        out = np.empty((rows, w.ld), dtype=self.host[0].dtype)
+        code = {"f32": oracle.F32, "bf16": oracle.BF16, "f16": oracle.F16, "i32": oracle.I32}[self.storage]
+        ops = {"sum": oracle.SUM, "max": oracle.MAX, "min": oracle.MIN}
+        bounds = [rows * t // threads for t in range(threads + 1)]
+
+        def part(t):
+            lo, hi = bounds[t], bounds[t + 1]
+            for op in w.ops:
+                oracle.treduce([h[lo:hi] for h in self.host], out[lo:hi], hi - lo, w.valid_cols, w.ld,
+                               ops[op], code)
+
+        with ThreadPoolExecutor(threads) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(part, range(threads)))
+            dt = time.perf_counter() - t0
+        nbytes = (w.nranks + 1) * w.elem_bytes * rows * w.valid_cols * len(w.ops)
+        return nbytes, dt, out
+
 
 class RsAgBench(Workload):
     """reduce_scatter (Sum) then allgather over 8 fp16 windows [8192, 4096]."""
@@ -825,8 +852,20 @@ def cpu_baseline(wl, budget_s):
     while dt_tot < budget_s or reps == 0:
         nb, dt, desc = wl.oracle_sample(rows)
         nb_tot, dt_tot, reps = nb_tot + nb, dt_tot + dt, reps + 1
-    return {"value": nb_tot / dt_tot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    line = {"value": nb_tot / dt_tot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%s, %d repetition(s)" % (desc, reps), "seconds": round(dt_tot, 3)}
+    if hasattr(wl, "oracle_sample_threaded"):
+        # the same oracle over every host core, rows split into contiguous slices
+        threads = os.cpu_count() or 1
+        n_rows = max(threads, int(rps * threads * budget_s / 4))
+        nb_t, dt_t, reps_t = 0, 0.0, 0
+        while dt_t < budget_s / 4 or reps_t == 0:
+            nb, dt, _ = wl.oracle_sample_threaded(n_rows, threads)
+            nb_t, dt_t, reps_t = nb_t + nb, dt_t + dt, reps_t + 1
+        line["all_cores"] = {"value": nb_t / dt_t / 1e9, "cores": threads, "seconds": round(dt_t, 3),
+                             "sample": "the first %d rows, split into %d row slices on as many threads, "
+                             "%d repetition(s)" % (min(n_rows, wl.w.valid_rows), threads, reps_t)}
+    return line
 
 
 def run_ours(args):

@@ -64,3 +64,24 @@ def test_defaults_and_reference_line():
         assert key in line
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_threaded_oracle_sample_matches_one_call():
+    """The all-cores CPU baseline splits rows over threads; its result equals
+    one oracle call over the same rows, byte for byte."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    wl = bench.make_workload("treduce_small")
+    wl.setup_host()
+    w = wl.w
+    rows = 37
+    ref = np.empty((rows, w.ld), dtype=wl.host[0].dtype)
+    nb, dt, got = wl.oracle_sample_threaded(rows, 5)
+    for op in w.ops:
+        oracle.treduce(wl.host, ref, rows, w.valid_cols, w.ld, {"sum": oracle.SUM, "max": oracle.MAX,
+                                                                 "min": oracle.MIN}[op], oracle.F32)
+    assert got.shape == ref.shape
+    assert np.array_equal(got[:, :w.valid_cols].view(np.uint32), ref[:, :w.valid_cols].view(np.uint32))
+    assert nb == (w.nranks + 1) * 4 * rows * w.valid_cols * len(w.ops)
