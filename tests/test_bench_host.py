@@ -85,3 +85,18 @@ def test_threaded_oracle_sample_matches_one_call():
     assert got.shape == ref.shape
     assert np.array_equal(got[:, :w.valid_cols].view(np.uint32), ref[:, :w.valid_cols].view(np.uint32))
     assert nb == (w.nranks + 1) * 4 * rows * w.valid_cols * len(w.ops)
+
+
+def test_traffic_source_lists_exist():
+    """Every kernel source a traffic record is keyed to exists, and the lists
+    cover every device-code file of the library."""
+    import glob
+    sys.path.insert(0, ROOT)
+    import bench
+    listed = set(bench.REDUCE_SOURCES) | set(bench.MOVE_SOURCES)
+    for rel in listed:
+        assert os.path.exists(os.path.join(ROOT, rel)), rel
+    csrc = os.path.join(ROOT, "tile_level_collective_gb300", "csrc")
+    device = {os.path.relpath(f, ROOT) for f in glob.glob(os.path.join(csrc, "*"))
+              if f.endswith((".cuh", ".h")) or os.path.basename(f).startswith(("reduce_", "movement"))}
+    assert device <= listed, device - listed

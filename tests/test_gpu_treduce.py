@@ -283,15 +283,12 @@ def test_workload_3_i32_max_full_size():
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("variant", ["vec", "async"])
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 @pytest.mark.parametrize("op", ["sum", "max", "min"])
-def test_both_kernels_on_aligned_data(variant, dtype, op, monkeypatch):
-    """16-byte-aligned data runs the shared-memory pipeline by default; the
-    register kernel (the path for narrower alignment) is forced here through
-    the library's PTOC_VARIANT switch so both stay covered on the same cases,
-    with more than one group of eight ranks and ragged rows."""
-    monkeypatch.setenv("PTOC_VARIANT", variant)
+def test_aligned_data_group_forms(dtype, op):
+    """16-byte-aligned data: more than one group of eight ranks (the kernel's
+    multi-group form, with ragged rows and row tails), one group on full rows,
+    and the in-place form."""
     run_case(dtype, op, 11, 7, 520, 528, 6, 517, root=4, seed=12, specials=True)
     run_case(dtype, op, 8, 33, 256, 256, 33, 256, root=0, seed=13)       # flat, full rows
     run_case(dtype, op, 2, 3, 64, 64, 3, 64, root=1, seed=14, inplace=True)

@@ -32,12 +32,10 @@ AR_CASES = [
 ]
 
 
-@pytest.mark.parametrize("variant", ["async", "vec"])
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
 @pytest.mark.parametrize("op", ["sum", "max", "min", "prod"])
 @pytest.mark.parametrize("case", AR_CASES, ids=lambda c: "n%d_%dx%d_ld%d_o%d" % c)
-def test_allreduce_small(variant, dtype, op, case, monkeypatch):
-    monkeypatch.setenv("PTOC_VARIANT", variant)
+def test_allreduce_small(dtype, op, case):
     n, rows, cols, ld, off = case
     host = windows_host(dtype, n, rows, cols, ld, seed=rows * 7 + n)
     orig = [h.copy() for h in host]

@@ -15,10 +15,12 @@
 // leg: rank d pushes the recv_counts[d][s] rows it holds from s back to s's
 // output, overwriting or adding. Because the rows of one pair are contiguous
 // on both sides, each pair is one contiguous copy of c * row_bytes bytes. The
-// counts live on the device, so the grid cannot be sized from them: a
-// persistent grid walks a list of fixed-size tiles, and every CTA rebuilds the
-// per-pair tile prefix sums in shared memory from the N^2 counts (a few
-// hundred integers, L2-resident) before it starts.
+// counts live on the device, so the grid is sized for the largest possible
+// run: grid.y is the pair, grid.x the tile of the pair's run, one tile per
+// block. A block reads its pair's count (one L2-resident integer), publishes
+// it if it is the pair's first block, and exits at once when its tile lies
+// past the run; the hardware block scheduler hands out the live tiles in
+// order as blocks retire.
 #include <cuda_runtime.h>
 
 #include "ptoc_internal.h"
@@ -98,58 +100,6 @@ __device__ __forceinline__ int32_t clamp_count(int32_t c, int64_t max_recv)
     return (int32_t)(v > max_recv ? max_recv : v);
 }
 
-// Per-pair state in shared memory: cnt[q] = clamped count of pair q
-// (q = a * N + b), pre[q] = tiles of pairs 0..q-1 (exclusive prefix), pre[np]
-// = total. Each thread scans a contiguous run of pairs; the run totals are
-// combined with a warp-shuffle scan and a pass over the warp totals. Block 0
-// also publishes the counts when asked (all_to_all_v's recv_counts).
-__device__ void build_pairs(const A2avParams& p, int32_t* cnt, int32_t* pre, int32_t* warp_tot)
-{
-    const int n = p.nranks;
-    const int np = n * n;
-    const int per = (np + kBlock - 1) / kBlock;
-    const int q0 = threadIdx.x * per;
-    const int q1 = min(q0 + per, np);
-
-    int32_t run = 0;
-    for (int q = q0; q < q1; ++q) {
-        const int a = q / n, b = q - (q / n) * n;
-        const int32_t c = p.full ? (int32_t)p.max_recv : clamp_count(p.cnt[a][b], p.max_recv);
-        if (p.publish && blockIdx.x == 0) p.pub[b][a] = c;
-        cnt[q] = c;
-        const int32_t tiles = (int32_t)(((int64_t)c * p.row_bytes + p.tile_bytes - 1) / p.tile_bytes);
-        pre[q] = tiles;                 // temporarily: this pair's tile count
-        run += tiles;
-    }
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int32_t incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t acc = 0;
-        for (int w = 0; w < kBlock / 32; ++w) {
-            const int32_t t = warp_tot[w];
-            warp_tot[w] = acc;
-            acc += t;
-        }
-        pre[np] = acc;
-    }
-    __syncthreads();
-    int32_t excl = warp_tot[warp] + incl - run;   // tiles before this thread's run
-    for (int q = q0; q < q1; ++q) {
-        const int32_t tiles = pre[q];
-        pre[q] = excl;
-        excl += tiles;
-    }
-    __syncthreads();
-}
-
 // Moves one chunk of VB bytes: a copy, or (AddMover) out += in per element.
 template <int VB>
 struct CopyMover {
@@ -190,35 +140,27 @@ struct AddMover1 {
 };
 
 // U chunks of VB bytes per thread per tile: tile_bytes = U * kBlock * VB.
+// Block (x, q) moves bytes [x * tile_bytes, (x + 1) * tile_bytes) of pair
+// q = a * N + b: from input a, rows b * MAX_RECV .., to output b, rows
+// a * MAX_RECV .. (a grid-stride loop over x covers grids capped below the
+// run's tile count).
 template <class M, int VB, int U>
 __global__ void __launch_bounds__(kBlock) pairs_kernel(const __grid_constant__ A2avParams p)
 {
-    extern __shared__ int32_t smem[];
-    __shared__ int32_t warp_tot[kBlock / 32];
     const int n = p.nranks;
-    const int np = n * n;
-    int32_t* cnt = smem;                    // np entries
-    int32_t* pre = smem + np;               // np + 1 entries
+    const int q = blockIdx.y;
+    const int a = q / n, b = q - a * n;
     pdl_enter();
-    build_pairs(p, cnt, pre, warp_tot);
-    const int32_t total = pre[np];
+    const int32_t c = p.full ? (int32_t)p.max_recv : clamp_count(p.cnt[a][b], p.max_recv);
+    if (p.publish && blockIdx.x == 0 && threadIdx.x == 0) p.pub[b][a] = c;
+    const int64_t bytes = (int64_t)c * p.row_bytes;
+    const char* src0 = (const char*)p.in[a] + b * p.max_recv * p.row_bytes;
+    char* dst0 = (char*)p.out[b] + a * p.max_recv * p.row_bytes;
 
-    for (int32_t t = blockIdx.x; t < total; t += gridDim.x) {
-        // the pair q with pre[q] <= t < pre[q + 1]
-        int lo = 0, hi = np;                // invariant: pre[lo] <= t < pre[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (pre[mid] <= t) lo = mid;
-            else hi = mid;
-        }
-        const int q = lo;
-        const int a = q / n, b = q - (q / n) * n;
-        const int64_t bytes = (int64_t)cnt[q] * p.row_bytes;
-        const int64_t beg = (int64_t)(t - pre[q]) * p.tile_bytes;
+    for (int64_t beg = (int64_t)blockIdx.x * p.tile_bytes; beg < bytes; beg += (int64_t)gridDim.x * p.tile_bytes) {
         const int64_t len = min(p.tile_bytes, bytes - beg);
-        const char* src = (const char*)p.in[a] + b * p.max_recv * p.row_bytes + beg;
-        char* dst = (char*)p.out[b] + a * p.max_recv * p.row_bytes + beg;
-
+        const char* src = src0 + beg;
+        char* dst = dst0 + beg;
         typename M::V x[U];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
@@ -233,44 +175,19 @@ __global__ void __launch_bounds__(kBlock) pairs_kernel(const __grid_constant__ A
     }
 }
 
-size_t a2av_smem_bytes(int nranks) { return (size_t)(2 * nranks * nranks + 1) * sizeof(int32_t); }
-
 template <int U>
 static cudaError_t launch_a2av_u(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
-    const size_t smem = a2av_smem_bytes(p.nranks);
-    if (vb == 16) return launch_kernel(pairs_kernel<CopyMover<16>, 16, U>, grid, kBlock, smem, s, p);
-    if (vb == 8) return launch_kernel(pairs_kernel<CopyMover<8>, 8, U>, grid, kBlock, smem, s, p);
-    if (vb == 4) return launch_kernel(pairs_kernel<CopyMover<4>, 4, U>, grid, kBlock, smem, s, p);
-    return launch_kernel(pairs_kernel<CopyMover<2>, 2, U>, grid, kBlock, smem, s, p);
+    if (vb == 16) return launch_kernel(pairs_kernel<CopyMover<16>, 16, U>, grid, kBlock, 0, s, p);
+    if (vb == 8) return launch_kernel(pairs_kernel<CopyMover<8>, 8, U>, grid, kBlock, 0, s, p);
+    if (vb == 4) return launch_kernel(pairs_kernel<CopyMover<4>, 4, U>, grid, kBlock, 0, s, p);
+    return launch_kernel(pairs_kernel<CopyMover<2>, 2, U>, grid, kBlock, 0, s, p);
 }
 
 cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s)
 {
-    return unroll == 8 ? launch_a2av_u<8>(p, vb, grid, s) : launch_a2av_u<4>(p, vb, grid, s);
-}
-
-template <class K>
-static int occupancy_of_kernel(K kernel, size_t smem)
-{
-    int b = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kBlock, smem);
-    return (e == cudaSuccess && b > 0) ? b : 1;
-}
-
-template <int U>
-static int a2av_occupancy_u(int vb, size_t smem)
-{
-    return vb == 16 ? occupancy_of_kernel(pairs_kernel<CopyMover<16>, 16, U>, smem)
-         : vb == 8 ? occupancy_of_kernel(pairs_kernel<CopyMover<8>, 8, U>, smem)
-         : vb == 4 ? occupancy_of_kernel(pairs_kernel<CopyMover<4>, 4, U>, smem)
-                   : occupancy_of_kernel(pairs_kernel<CopyMover<2>, 2, U>, smem);
-}
-
-int a2av_blocks_per_sm(int vb, int unroll, int nranks)
-{
-    const size_t smem = a2av_smem_bytes(nranks);
-    return unroll == 8 ? a2av_occupancy_u<8>(vb, smem) : a2av_occupancy_u<4>(vb, smem);
+    if (unroll == 16) return launch_a2av_u<16>(p, vb, grid, s);
+    return unroll == 4 ? launch_a2av_u<4>(p, vb, grid, s) : launch_a2av_u<8>(p, vb, grid, s);
 }
 
 // The combine with kAdd: 4 chunks per thread per tile (each chunk loads both
@@ -280,12 +197,11 @@ constexpr int kAddUnroll = 4;
 template <class T>
 static cudaError_t launch_add_t(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
-    const size_t smem = a2av_smem_bytes(p.nranks);
-    if (vb == 16) return launch_kernel(pairs_kernel<AddMover<T, 16>, 16, kAddUnroll>, grid, kBlock, smem, s, p);
-    if (vb == 8) return launch_kernel(pairs_kernel<AddMover<T, 8>, 8, kAddUnroll>, grid, kBlock, smem, s, p);
-    if (vb == 4) return launch_kernel(pairs_kernel<AddMover<T, 4>, 4, kAddUnroll>, grid, kBlock, smem, s, p);
+    if (vb == 16) return launch_kernel(pairs_kernel<AddMover<T, 16>, 16, kAddUnroll>, grid, kBlock, 0, s, p);
+    if (vb == 8) return launch_kernel(pairs_kernel<AddMover<T, 8>, 8, kAddUnroll>, grid, kBlock, 0, s, p);
+    if (vb == 4) return launch_kernel(pairs_kernel<AddMover<T, 4>, 4, kAddUnroll>, grid, kBlock, 0, s, p);
     if constexpr (sizeof(T) == 2)
-        return launch_kernel(pairs_kernel<AddMover1<T>, 2, kAddUnroll>, grid, kBlock, smem, s, p);
+        return launch_kernel(pairs_kernel<AddMover1<T>, 2, kAddUnroll>, grid, kBlock, 0, s, p);
     return cudaErrorInvalidValue;
 }
 
@@ -296,27 +212,6 @@ cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, 
     case PTOC_I32: return launch_add_t<int32_t>(p, vb, grid, s);
     case PTOC_F16: return launch_add_t<__half>(p, vb, grid, s);
     default: return launch_add_t<__nv_bfloat16>(p, vb, grid, s);
-    }
-}
-
-template <class T>
-static int add_occupancy_t(int vb, size_t smem)
-{
-    if (vb == 16) return occupancy_of_kernel(pairs_kernel<AddMover<T, 16>, 16, kAddUnroll>, smem);
-    if (vb == 8) return occupancy_of_kernel(pairs_kernel<AddMover<T, 8>, 8, kAddUnroll>, smem);
-    if (vb == 4) return occupancy_of_kernel(pairs_kernel<AddMover<T, 4>, 4, kAddUnroll>, smem);
-    if constexpr (sizeof(T) == 2) return occupancy_of_kernel(pairs_kernel<AddMover1<T>, 2, kAddUnroll>, smem);
-    return 1;
-}
-
-int pairs_add_blocks_per_sm(int dtype, int vb, int nranks)
-{
-    const size_t smem = a2av_smem_bytes(nranks);
-    switch (dtype) {
-    case PTOC_F32: return add_occupancy_t<float>(vb, smem);
-    case PTOC_I32: return add_occupancy_t<int32_t>(vb, smem);
-    case PTOC_F16: return add_occupancy_t<__half>(vb, smem);
-    default: return add_occupancy_t<__nv_bfloat16>(vb, smem);
     }
 }
 

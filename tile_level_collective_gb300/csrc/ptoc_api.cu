@@ -98,61 +98,14 @@ int sm_count()
     return c;
 }
 
-// Optional A/B switch for measurements: PTOC_VARIANT=vec forces the register
-// kernel on 16-byte-aligned data (default: the shared-memory pipeline).
-bool use_async_variant()
-{
-    const char* e = getenv("PTOC_VARIANT");
-    return !(e && strcmp(e, "vec") == 0);
-}
-
-// Pipeline shape of the shared-memory kernel: PTOC_ASYNC_CFG=<index> into
-// the shape table (A/B switch for measurements; 0 is the default shape).
-int async_cfg()
-{
-    const char* e = getenv("PTOC_ASYNC_CFG");
-    if (e && e[0] >= '0' && e[0] < '0' + kAsyncCfgs && e[1] == 0) return e[0] - '0';
-    return 0;
-}
-
-// Chunks per thread per all_to_all_v tile: PTOC_A2AV_UNROLL=4|8 (A/B
-// switch for measurements; default 8).
+// Chunks per thread per all_to_all_v tile: PTOC_A2AV_UNROLL=4|8|16 (A/B
+// switch for measurements; default 8, 32 KB tiles for 16-byte vectors).
 int a2av_unroll()
 {
     const char* e = getenv("PTOC_A2AV_UNROLL");
-    return (e && strcmp(e, "4") == 0) ? 4 : 8;
-}
-
-int async_occupancy(int dtype, int op, int cfg)
-{
-    const int dev = current_device();
-    switch (dtype) {
-    case PTOC_F32: return occupancy_async_f32(op, cfg, dev);
-    case PTOC_I32: return occupancy_async_i32(op, cfg, dev);
-    case PTOC_F16: return occupancy_async_f16(op, cfg, dev);
-    default: return occupancy_async_bf16(op, cfg, dev);
-    }
-}
-
-cudaError_t launch_async(int dtype, const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s)
-{
-    switch (dtype) {
-    case PTOC_F32: return launch_async_f32(p, op, cfg, grid, s);
-    case PTOC_I32: return launch_async_i32(p, op, cfg, grid, s);
-    case PTOC_F16: return launch_async_f16(p, op, cfg, grid, s);
-    default: return launch_async_bf16(p, op, cfg, grid, s);
-    }
-}
-
-// Optional A/B switch for measurements: PTOC_UNROLL=1|2 (vectors per thread
-// per tile in the reductions). Default 1: 2 doubles the registers of the
-// 16-byte kernels (one resident CTA per SM instead of two) for the same bytes
-// in flight per SM.
-int reduce_unroll(int vb)
-{
-    const char* e = getenv("PTOC_UNROLL");
-    if (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) return e[0] - '0';
-    return 1;
+    if (e && strcmp(e, "4") == 0) return 4;
+    if (e && strcmp(e, "16") == 0) return 16;
+    return 8;
 }
 
 // Tile description of a [rows, cols] box with pitch ld for vectors of vb
@@ -184,47 +137,31 @@ dim3 grid_for(int64_t ntiles)
     return dim3((unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap));
 }
 
-cudaError_t launch_reduce_regs(int dtype, const ReduceParams& p, int op, int vb, int unroll, dim3 grid,
-                               cudaStream_t s)
+cudaError_t launch_reduce_regs(int dtype, const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s)
 {
     switch (dtype) {
-    case PTOC_F32: return launch_reduce_f32(p, op, vb, unroll, grid, s);
-    case PTOC_I32: return launch_reduce_i32(p, op, vb, unroll, grid, s);
-    case PTOC_F16: return launch_reduce_f16(p, op, vb, unroll, grid, s);
-    default: return launch_reduce_bf16(p, op, vb, unroll, grid, s);
+    case PTOC_F32: return launch_reduce_f32(p, op, vb, grid, s);
+    case PTOC_I32: return launch_reduce_i32(p, op, vb, grid, s);
+    case PTOC_F16: return launch_reduce_f16(p, op, vb, grid, s);
+    default: return launch_reduce_bf16(p, op, vb, grid, s);
     }
 }
 
 // Tile a [rows, cols] box with pitch ld and launch one reduction over it
-// (p.src, p.dst, p.nranks and p.dst_mode already filled in): the
-// shared-memory pipeline when every address and the pitch are 16-byte
-// aligned, the register kernel otherwise.
+// (p.src, p.dst, p.nranks and p.dst_mode already filled in): one block per
+// tile of kBlock vectors of vb bytes, then the row-tail blocks.
 cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, int64_t cols, int64_t ld,
                              int eb, int vb, cudaStream_t s)
 {
     p.ld = ld;
     p.rows = rows;
-    if (vb == 16 && use_async_variant()) {
-        const int cfg = async_cfg();
-        const int occ = async_occupancy(dtype, op, cfg);
-        if (occ > 0) {
-            const Box b = make_box(rows, cols, ld, eb, 16, kAsyncB[cfg]);
-            p.vpr = b.vpr;
-            p.tail = b.tail;
-            p.tpr = b.tpr;
-            p.ntiles = b.ntiles;
-            const int64_t want = (int64_t)sm_count() * occ;
-            const int grid = (int)(want < b.ntiles ? want : b.ntiles);
-            return launch_async(dtype, p, op, cfg, grid, s);
-        }
-    }
-    const int unroll = reduce_unroll(vb);
-    const Box b = make_box(rows, cols, ld, eb, vb, kBlock * unroll);
+    const Box b = make_box(rows, cols, ld, eb, vb, kBlock);
     p.vpr = b.vpr;
     p.tail = b.tail;
     p.tpr = b.tpr;
     p.ntiles = b.ntiles;
-    return launch_reduce_regs(dtype, p, op, vb, unroll, grid_for(p.ntiles), s);
+    p.tail_blocks = b.tail > 0 ? (rows * b.tail + kBlock - 1) / kBlock : 0;
+    return launch_reduce_regs(dtype, p, op, vb, grid_for(p.ntiles + p.tail_blocks), s);
 }
 
 ptoc_status check_group(const ptoc_group* g, bool need_root)
@@ -298,11 +235,13 @@ ptoc_status launch_pairs(A2avParams& p, const void* const* a, const void* const*
     const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
     const int unroll = add ? 4 : a2av_unroll();
     p.tile_bytes = (int64_t)vb * kBlock * unroll;
-    // tile indices are int32 in the kernel
-    const int64_t fp = p.max_recv * n * p.row_bytes;
-    if ((int64_t)n * (fp / p.tile_bytes + 1) + (int64_t)n * n >= INT32_MAX) return PTOC_ERR_UNSUPPORTED;
-    const int per_sm = add ? pairs_add_blocks_per_sm(dtype, vb, n) : a2av_blocks_per_sm(vb, unroll, n);
-    const dim3 grid((unsigned)(sm_count() * per_sm));
+    // grid.y = the N^2 pairs, grid.x = the tiles of the longest possible run
+    // (MAX_RECV rows); blocks past their pair's run exit at once
+    const int64_t run = p.max_recv * p.row_bytes;
+    int64_t gx = (run + p.tile_bytes - 1) / p.tile_bytes;
+    const int64_t cap = (int64_t)1 << 30;
+    gx = gx < 1 ? 1 : (gx > cap ? cap : gx);
+    const dim3 grid((unsigned)gx, (unsigned)(n * n));
     const cudaError_t e = add ? launch_pairs_add(p, dtype, vb, grid, stream) : launch_a2av(p, vb, unroll, grid, stream);
     return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }

@@ -20,19 +20,9 @@ enum Op : int { kSum = 0, kMax = 1, kMin = 2, kProd = 3 };
 // (reduce_scatter), or every window (allreduce).
 enum DstMode : int { kDstOne = 0, kDstOwner = 1, kDstAll = 2 };
 
-// Shapes of the shared-memory-pipelined reduction: S stages of G ranks, CTAs
-// of B threads (one tile = B vectors of 16 bytes). Shared memory per CTA is
-// S * G * B * 16 bytes. Index 0 is the default; PTOC_ASYNC_CFG=<index>
-// selects another one for measurements.
-constexpr int kAsyncCfgs = 6;
-constexpr int kAsyncS[kAsyncCfgs] = {2, 3, 2, 3, 4, 2};
-constexpr int kAsyncG[kAsyncCfgs] = {8, 8, 8, 8, 4, 16};
-constexpr int kAsyncB[kAsyncCfgs] = {256, 256, 128, 128, 256, 256};
-constexpr size_t async_smem_bytes(int cfg) { return (size_t)kAsyncS[cfg] * kAsyncG[cfg] * kAsyncB[cfg] * 16; }
-
 // TREDUCE and reduce_scatter. The box is `rows` rows of `vpr` full vectors of
 // VB bytes plus `tail` trailing elements; one tile is one row segment of
-// kBlock * U vectors (the last segment of a row also owns the tail).
+// kBlock vectors; the row tails are reduced by tail_blocks extra blocks.
 struct ReduceParams {
     const void* src[kMaxRanks];   // sources in reduction order (root first)
     void* dst[kMaxRanks];         // dst[0] for TREDUCE; window r for reduce_scatter / allreduce
@@ -41,6 +31,7 @@ struct ReduceParams {
     int64_t vpr;                  // full vectors per row
     int64_t tpr;                  // tiles per row
     int64_t ntiles;               // rows * tpr
+    int64_t tail_blocks;          // blocks after the tiles that reduce the row tails
     int32_t tail;                 // elements after the last full vector of a row
     int32_t nranks;
     int32_t dst_mode;             // DstMode
@@ -74,7 +65,7 @@ struct A2avParams {
     int32_t* pub[kMaxRanks];
     int64_t max_recv;             // target_rows / nranks
     int64_t row_bytes;            // size * element bytes
-    int64_t tile_bytes;
+    int64_t tile_bytes;           // bytes one block moves (the last tile of a run is shorter)
     int32_t nranks;
     int32_t full;                 // 1: every count is MAX_RECV
     int32_t publish;              // 1: write pub[b][a]
@@ -104,33 +95,15 @@ bool programmatic_launch();
 // Launchers (one translation unit per element type for the reductions).
 // `vb` is the vector width in bytes (16, 8 or 4; 2 for 16-bit data that is
 // only 2-byte aligned). They return the launch status; they never allocate.
-cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
-cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
-cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
-cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
+cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s);
 // The combine with AtomicType kAdd: out += in per element (binary32 for
 // floating types, one RNE narrowing; int32 wraps).
 cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, cudaStream_t s);
-int pairs_add_blocks_per_sm(int dtype, int vb, int nranks);
 
-// Shared-memory-pipelined reduction (16-byte-aligned data): persistent grid.
-cudaError_t launch_async_f32(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
-cudaError_t launch_async_i32(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
-cudaError_t launch_async_f16(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
-cudaError_t launch_async_bf16(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s);
-int occupancy_async_f32(int op, int cfg, int dev);
-int occupancy_async_i32(int op, int cfg, int dev);
-int occupancy_async_f16(int op, int cfg, int dev);
-int occupancy_async_bf16(int op, int cfg, int dev);
-
-// Resident CTAs per SM for each kernel (occupancy query).
-int occupancy_reduce_f32(int op, int vb, int unroll);
-int occupancy_reduce_i32(int op, int vb, int unroll);
-int occupancy_reduce_f16(int op, int vb, int unroll);
-int occupancy_reduce_bf16(int op, int vb, int unroll);
-int a2av_blocks_per_sm(int vb, int unroll, int nranks);
-size_t a2av_smem_bytes(int nranks);
 
 }  // namespace ptoc

@@ -1,37 +1,12 @@
 // TREDUCE / reduce_scatter / allreduce kernels for __nv_bfloat16 elements (one translation unit
 // per element type so the library builds in parallel).
-#include <atomic>
-
-#include "reduce_async.cuh"
 #include "reduce_impl.cuh"
 
 namespace ptoc {
 
-cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s)
+cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s)
 {
-    return launch_reduce_t<__nv_bfloat16>(p, op, vb, unroll, grid, s);
-}
-
-int occupancy_reduce_bf16(int op, int vb, int unroll) { return occupancy_t<__nv_bfloat16>(op, vb, unroll); }
-
-cudaError_t launch_async_bf16(const ReduceParams& p, int op, int cfg, int grid, cudaStream_t s)
-{
-    return launch_async_t<__nv_bfloat16>(p, op, cfg, grid, s);
-}
-
-// Resident CTAs per SM of the pipelined kernel on device `dev`, cached; the
-// first query of a device also opts the kernel into its shared-memory size.
-int occupancy_async_bf16(int op, int cfg, int dev)
-{
-    static std::atomic<int> cache[kMaxDevices][4][kAsyncCfgs];
-    if (dev < 0 || dev >= kMaxDevices || op < 0 || op > 3 || cfg < 0 || cfg >= kAsyncCfgs)
-        return async_occupancy_t<__nv_bfloat16>(op, cfg);
-    int v = cache[dev][op][cfg].load(std::memory_order_relaxed);
-    if (v == 0) {
-        v = async_occupancy_t<__nv_bfloat16>(op, cfg);
-        cache[dev][op][cfg].store(v > 0 ? v : -1, std::memory_order_relaxed);
-    }
-    return v > 0 ? v : 0;
+    return launch_reduce_t<__nv_bfloat16>(p, op, vb, grid, s);
 }
 
 }  // namespace ptoc

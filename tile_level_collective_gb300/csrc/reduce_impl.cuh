@@ -11,11 +11,13 @@
 //
 // How (GB300 design, not the page's UB ping-pong): the op is HBM-bound
 // (N reads + 1 write per element, at most one ALU op per loaded element), so
-// the kernel is a streaming engine. Each thread owns U vectors of VB bytes of
-// one row segment; it issues the loads of a group of up to kGroup ranks
-// back-to-back (U * kGroup independent 16-byte loads in flight per thread) and
-// only then folds them into its accumulator in rank order, so the loads of
-// later ranks overlap the reduction of earlier ones. Accumulation is binary32
+// the kernel is a streaming engine. Each block reduces one tile (a row
+// segment of kBlock vectors of VB bytes, one per thread); each thread issues
+// the loads of a group of up to kGroup ranks back to back (kGroup independent
+// 16-byte loads in flight per thread) and only then folds them into its
+// accumulator in rank order. The grid has one block per tile, so as blocks
+// retire the hardware block scheduler hands the next tiles, in order, to
+// whichever SM has room. Accumulation is binary32
 // for every floating type (one RNE narrowing at the store); 16-bit Max / Min
 // compare packed pairs and select the raw encodings, so their result is the
 // selected input bit for bit.
@@ -436,157 +438,126 @@ cudaError_t launch_kernel(K kernel, dim3 grid, unsigned block, size_t smem, cuda
 
 // ---- the kernel --------------------------------------------------------------
 
-template <class T, int OP, int VB, int U>
-__device__ __forceinline__ void reduce_vectors(const ReduceParams& p)
+// One tile: kBlock vectors of VB bytes of one row segment, one per thread.
+// The loads of a group of up to kGroup ranks are issued back to back, then
+// folded into the accumulator in rank order. MULTI instantiations (more than
+// kGroup ranks) repeat that for the following groups; the single-group
+// instantiation leaves the loop out, which keeps its register footprint low
+// enough for four resident blocks per SM.
+template <class T, int OP, int VB, bool MULTI>
+__device__ __forceinline__ void reduce_vector_tile(const ReduceParams& p, int64_t t)
 {
     constexpr int W = VB / 4;
-    constexpr int VE = VB / (int)sizeof(T);        // elements per vector
-    constexpr int TV = kBlock * U;                 // vectors per tile
     const int n = p.nranks;
+    const int64_t row = t / p.tpr;
+    const int64_t seg = t - row * p.tpr;
+    const int64_t v = seg * kBlock + threadIdx.x;
+    if (v >= p.vpr) return;
+    const int64_t off = row * p.ld * (int64_t)sizeof(T) + v * VB;
 
-    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const int64_t row = t / p.tpr;
-        const int64_t seg = t - row * p.tpr;
-        const int64_t row_elem = row * p.ld;
-        const int64_t v0 = seg * TV + threadIdx.x;
-
-        // byte offsets of this thread's U vectors (negative = inactive)
-        int64_t off[U];
+    VecAcc<T, OP, W> acc;
+    {
+        Words<W> x[kGroup];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            const int64_t v = v0 + (int64_t)k * kBlock;
-            off[k] = (v < p.vpr) ? (row_elem * (int64_t)sizeof(T) + v * VB) : -1;
-        }
-
-        VecAcc<T, OP, W> acc[U];
-        {
-            Words<W> x[kGroup][U];
+        for (int j = 0; j < kGroup; ++j)
+            if (j < n) x[j] = load_words<W>((const char*)p.src[j] + off);
+        acc.init(x[0]);
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j)
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (j < n && off[k] >= 0) x[j][k] = load_words<W>((const char*)p.src[j] + off[k]);
-#pragma unroll
-            for (int k = 0; k < U; ++k)
-                if (off[k] >= 0) acc[k].init(x[0][k]);
-#pragma unroll
-            for (int j = 1; j < kGroup; ++j)
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (j < n && off[k] >= 0) acc[k].add(x[j][k]);
-        }
+        for (int j = 1; j < kGroup; ++j)
+            if (j < n) acc.add(x[j]);
+    }
+    if constexpr (MULTI) {
         for (int g0 = kGroup; g0 < n; g0 += kGroup) {
-            Words<W> x[kGroup][U];
+            Words<W> x[kGroup];
 #pragma unroll
             for (int j = 0; j < kGroup; ++j)
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (g0 + j < n && off[k] >= 0) x[j][k] = load_words<W>((const char*)p.src[g0 + j] + off[k]);
+                if (g0 + j < n) x[j] = load_words<W>((const char*)p.src[g0 + j] + off);
 #pragma unroll
             for (int j = 0; j < kGroup; ++j)
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (g0 + j < n && off[k] >= 0) acc[k].add(x[j][k]);
-        }
-#pragma unroll
-        for (int k = 0; k < U; ++k)
-            if (off[k] >= 0) store_result<W>(p, row, off[k], acc[k].out());
-
-        // trailing elements of the row (fewer than one vector), owned by the
-        // row's last segment
-        if (p.tail > 0 && seg == p.tpr - 1) {
-            using Raw = typename Scalar<T>::Raw;
-            for (int c = threadIdx.x; c < p.tail; c += kBlock) {
-                const int64_t e = row_elem + p.vpr * VE + c;
-                store_elem<Raw>(p, row, e, reduce_one<T, OP>(p, e));
-            }
+                if (g0 + j < n) acc.add(x[j]);
         }
     }
+    store_result<W>(p, row, off, acc.out());
 }
 
-// One element per thread-slot: 16-bit data that is only 2-byte aligned.
-template <class T, int OP, int U>
-__device__ __forceinline__ void reduce_elements(const ReduceParams& p)
+// One element per thread: 16-bit data that is only 2-byte aligned (vpr is
+// then the row's element count and there is no tail).
+template <class T, int OP>
+__device__ __forceinline__ void reduce_element_tile(const ReduceParams& p, int64_t t)
 {
     using Raw = typename Scalar<T>::Raw;
-    constexpr int TV = kBlock * U;
-    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
-        const int64_t row = t / p.tpr;
-        const int64_t seg = t - row * p.tpr;
-#pragma unroll
-        for (int k = 0; k < U; ++k) {
-            const int64_t v = seg * TV + threadIdx.x + (int64_t)k * kBlock;
-            if (v < p.vpr) {
-                const int64_t e = row * p.ld + v;
-                store_elem<Raw>(p, row, e, reduce_one<T, OP>(p, e));
-            }
-        }
+    const int64_t row = t / p.tpr;
+    const int64_t seg = t - row * p.tpr;
+    const int64_t v = seg * kBlock + threadIdx.x;
+    if (v < p.vpr) {
+        const int64_t e = row * p.ld + v;
+        store_elem<Raw>(p, row, e, reduce_one<T, OP>(p, e));
     }
 }
 
-template <class T, int OP, int VB, int U>
+// Tail block b: the elements after the last full vector of each row (fewer
+// than one vector per row), rows * tail of them, one per thread.
+template <class T, int OP, int VB>
+__device__ __forceinline__ void reduce_tail_block(const ReduceParams& p, int64_t b)
+{
+    using Raw = typename Scalar<T>::Raw;
+    constexpr int VE = VB / (int)sizeof(T);
+    const int64_t i = b * kBlock + threadIdx.x;
+    if (i >= p.rows * p.tail) return;
+    const int64_t row = i / p.tail;
+    const int64_t c = i - row * p.tail;
+    const int64_t e = row * p.ld + p.vpr * VE + c;
+    store_elem<Raw>(p, row, e, reduce_one<T, OP>(p, e));
+}
+
+// Work item w < ntiles is vector tile w, the rest are tail blocks. The grid
+// normally has one block per work item, so the hardware block scheduler hands
+// out the tiles in order as blocks retire; a grid-stride loop covers grids
+// capped below the item count.
+template <class T, int OP, int VB, bool MULTI>
 __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ ReduceParams p)
 {
     pdl_enter();
-    if constexpr (VB < 4) {
-        reduce_elements<T, OP, U>(p);
-    } else {
-        reduce_vectors<T, OP, VB, U>(p);
+    const int64_t total = p.ntiles + p.tail_blocks;
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+        if (w < p.ntiles) {
+            if constexpr (VB < 4) reduce_element_tile<T, OP>(p, w);
+            else reduce_vector_tile<T, OP, VB, MULTI>(p, w);
+        } else {
+            if constexpr (VB >= 4) reduce_tail_block<T, OP, VB>(p, w - p.ntiles);
+        }
     }
 }
 
 template <class T, int OP, int VB>
-cudaError_t launch_reduce_vb(const ReduceParams& p, int unroll, dim3 grid, cudaStream_t s)
+cudaError_t launch_reduce_vb(const ReduceParams& p, dim3 grid, cudaStream_t s)
 {
-    if (unroll == 2) return launch_kernel(reduce_kernel<T, OP, VB, 2>, grid, kBlock, 0, s, p);
-    return launch_kernel(reduce_kernel<T, OP, VB, 1>, grid, kBlock, 0, s, p);
+    if (VB >= 4 && p.nranks > kGroup) return launch_kernel(reduce_kernel<T, OP, VB, true>, grid, kBlock, 0, s, p);
+    return launch_kernel(reduce_kernel<T, OP, VB, false>, grid, kBlock, 0, s, p);
 }
 
 template <class T, int OP>
-cudaError_t launch_reduce_op(const ReduceParams& p, int vb, int unroll, dim3 grid, cudaStream_t s)
+cudaError_t launch_reduce_op(const ReduceParams& p, int vb, dim3 grid, cudaStream_t s)
 {
     switch (vb) {
-    case 16: return launch_reduce_vb<T, OP, 16>(p, unroll, grid, s);
-    case 8: return launch_reduce_vb<T, OP, 8>(p, unroll, grid, s);
-    case 4: return launch_reduce_vb<T, OP, 4>(p, unroll, grid, s);
+    case 16: return launch_reduce_vb<T, OP, 16>(p, grid, s);
+    case 8: return launch_reduce_vb<T, OP, 8>(p, grid, s);
+    case 4: return launch_reduce_vb<T, OP, 4>(p, grid, s);
     default:
-        if constexpr (sizeof(T) == 2) return launch_reduce_vb<T, OP, 2>(p, unroll, grid, s);
+        if constexpr (sizeof(T) == 2) return launch_reduce_vb<T, OP, 2>(p, grid, s);
         return cudaErrorInvalidValue;
     }
 }
 
 template <class T>
-cudaError_t launch_reduce_t(const ReduceParams& p, int op, int vb, int unroll, dim3 grid, cudaStream_t s)
+cudaError_t launch_reduce_t(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s)
 {
     switch (op) {
-    case kSum: return launch_reduce_op<T, kSum>(p, vb, unroll, grid, s);
-    case kMax: return launch_reduce_op<T, kMax>(p, vb, unroll, grid, s);
-    case kProd: return launch_reduce_op<T, kProd>(p, vb, unroll, grid, s);
-    default: return launch_reduce_op<T, kMin>(p, vb, unroll, grid, s);
+    case kSum: return launch_reduce_op<T, kSum>(p, vb, grid, s);
+    case kMax: return launch_reduce_op<T, kMax>(p, vb, grid, s);
+    case kProd: return launch_reduce_op<T, kProd>(p, vb, grid, s);
+    default: return launch_reduce_op<T, kMin>(p, vb, grid, s);
     }
-}
-
-template <class T, int OP, int VB, int U>
-int occupancy_of()
-{
-    int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reduce_kernel<T, OP, VB, U>, kBlock, 0) != cudaSuccess)
-        return 1;
-    return b > 0 ? b : 1;
-}
-
-template <class T>
-int occupancy_t(int op, int vb, int unroll)
-{
-#define PTOC_OCC(OPV)                                                                   \
-    if (vb == 16) return unroll == 2 ? occupancy_of<T, OPV, 16, 2>() : occupancy_of<T, OPV, 16, 1>(); \
-    if (vb == 8) return unroll == 2 ? occupancy_of<T, OPV, 8, 2>() : occupancy_of<T, OPV, 8, 1>();    \
-    return unroll == 2 ? occupancy_of<T, OPV, 4, 2>() : occupancy_of<T, OPV, 4, 1>();
-    if (op == kSum) { PTOC_OCC(kSum) }
-    if (op == kMax) { PTOC_OCC(kMax) }
-    if (op == kProd) { PTOC_OCC(kProd) }
-    PTOC_OCC(kMin)
-#undef PTOC_OCC
 }
 
 }  // namespace ptoc
