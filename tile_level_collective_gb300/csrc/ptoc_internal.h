@@ -55,9 +55,8 @@ struct GatherParams {
 //   combine      : a = the rank that received, b = the original sender,
 //                  count = clamp(cnt[a][b]) with cnt = recv_counts; out is
 //                  overwritten or added into (AtomicType).
-// Each pair is one contiguous segment cut into tiles of tile_bytes; clamped
-// counts and tile prefix sums over pairs are built in shared memory per CTA
-// (int32: a launch moves fewer than 2^31 tiles).
+// Each pair is one contiguous segment cut into tiles of tile_bytes; block
+// (x, q) of the launch moves tile x of pair q and reads only q's count.
 struct A2avParams {
     const void* in[kMaxRanks];
     void* out[kMaxRanks];
