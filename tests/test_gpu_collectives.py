@@ -37,6 +37,8 @@ RS_CASES = [
     (5, 17, 1030, 1032, 4),
     (8, 9, 8200, 8200, 8),
     (6, 7, 31, 33, 0),        # odd pitch
+    (8, 100, 131, 136, 0),    # row tails of every owner, over two tail blocks
+    (9, 90, 131, 136, 0),     # two rank groups with row tails
 ]
 
 

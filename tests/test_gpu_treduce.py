@@ -112,6 +112,11 @@ SMALL = [
     (4, 6, 50, 52, 6, 50, 0, 4),                # 4-byte aligned buffers
     (4, 6, 50, 52, 6, 50, 2, 8),                # 8-byte aligned buffers
     (5, 7, 31, 33, 7, 31, 4, 0),                # odd pitch: narrow vectors
+    (5, 300, 515, 520, 300, 515, 2, 0),         # 900 row-tail elements: four tail blocks
+    (11, 120, 259, 264, 120, 259, 7, 0),        # two rank groups, tails over two tail blocks
+    (12, 5, 67, 72, 5, 67, 3, 4),               # 9-16 ranks on 4-byte-aligned buffers
+    (20, 4, 130, 136, 4, 129, 11, 8),           # over 16 ranks on 8-byte-aligned buffers
+    (16, 6, 520, 520, 6, 517, 15, 0),           # 16 ranks, 16-byte data narrowed to 8-byte vectors
 ]
 
 

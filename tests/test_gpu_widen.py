@@ -29,6 +29,8 @@ AR_CASES = [
     (9, 7, 520, 528, 0),       # two groups of ranks
     (5, 6, 100, 100, 4),
     (4, 5, 31, 33, 0),         # odd pitch
+    (8, 100, 131, 136, 0),     # row tails written to every window, two tail blocks
+    (10, 40, 67, 72, 0),       # two rank groups with row tails
 ]
 
 

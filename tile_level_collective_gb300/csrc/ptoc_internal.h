@@ -12,6 +12,7 @@ namespace ptoc {
 
 constexpr int kMaxRanks = PTOC_MAX_RANKS;
 constexpr int kBlock = 256;          // threads per CTA for every streaming kernel
+constexpr int kGroup = 8;            // ranks whose 16-byte loads a reduction thread issues together
 constexpr int kMaxDevices = 64;      // per-device caches
 
 enum Op : int { kSum = 0, kMax = 1, kMin = 2, kProd = 3 };

@@ -15,7 +15,8 @@
 // segment of kBlock vectors of VB bytes, one per thread); each thread issues
 // the loads of a group of up to kGroup ranks back to back (kGroup independent
 // 16-byte loads in flight per thread) and only then folds them into its
-// accumulator in rank order. The grid has one block per tile, so as blocks
+// accumulator in rank order (9 to 16 ranks: 8-byte vectors, all 16 loads in
+// flight; more ranks: one group after another). The grid has one block per tile, so as blocks
 // retire the hardware block scheduler hands the next tiles, in order, to
 // whichever SM has room. Accumulation is binary32
 // for every floating type (one RNE narrowing at the store); 16-bit Max / Min
@@ -33,7 +34,6 @@
 
 namespace ptoc {
 
-constexpr int kGroup = 8;   // ranks whose loads are issued together
 
 template <int W>
 struct Words {
@@ -438,16 +438,24 @@ cudaError_t launch_kernel(K kernel, dim3 grid, unsigned block, size_t smem, cuda
 
 // ---- the kernel --------------------------------------------------------------
 
-// One tile: kBlock vectors of VB bytes of one row segment, one per thread.
-// The loads of a group of up to kGroup ranks are issued back to back, then
-// folded into the accumulator in rank order. MULTI instantiations (more than
-// kGroup ranks) repeat that for the following groups; the single-group
-// instantiation leaves the loop out, which keeps its register footprint low
-// enough for four resident blocks per SM.
-template <class T, int OP, int VB, bool MULTI>
+// How a thread covers the ranks (chosen on the host from the rank count):
+//   kOneGroup  up to kGroup ranks: all loads issued back to back, then folded.
+//   kWide      up to 2 * kGroup ranks on vectors of at most 8 bytes: the same,
+//              with all 2 * kGroup loads in flight (the host narrows 16-byte
+//              vectors to 8 so the registers stay those of one group).
+//   kGroups    more ranks: groups of kGroup, each issued and then folded.
+enum RankForm : int { kOneGroup = 0, kWide = 1, kGroups = 2 };
+
+template <int FORM>
+constexpr int kSlots = FORM == kWide ? 2 * kGroup : kGroup;
+
+// One tile: kBlock vectors of VB bytes of one row segment, one per thread,
+// folded in rank order 0, 1, 2, ... whatever the form.
+template <class T, int OP, int VB, int FORM>
 __device__ __forceinline__ void reduce_vector_tile(const ReduceParams& p, int64_t t)
 {
     constexpr int W = VB / 4;
+    constexpr int S = kSlots<FORM>;
     const int n = p.nranks;
     const int64_t row = t / p.tpr;
     const int64_t seg = t - row * p.tpr;
@@ -457,23 +465,23 @@ __device__ __forceinline__ void reduce_vector_tile(const ReduceParams& p, int64_
 
     VecAcc<T, OP, W> acc;
     {
-        Words<W> x[kGroup];
+        Words<W> x[S];
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j)
+        for (int j = 0; j < S; ++j)
             if (j < n) x[j] = load_words<W>((const char*)p.src[j] + off);
         acc.init(x[0]);
 #pragma unroll
-        for (int j = 1; j < kGroup; ++j)
+        for (int j = 1; j < S; ++j)
             if (j < n) acc.add(x[j]);
     }
-    if constexpr (MULTI) {
-        for (int g0 = kGroup; g0 < n; g0 += kGroup) {
-            Words<W> x[kGroup];
+    if constexpr (FORM == kGroups) {
+        for (int g0 = S; g0 < n; g0 += S) {
+            Words<W> x[S];
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j)
+            for (int j = 0; j < S; ++j)
                 if (g0 + j < n) x[j] = load_words<W>((const char*)p.src[g0 + j] + off);
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j)
+            for (int j = 0; j < S; ++j)
                 if (g0 + j < n) acc.add(x[j]);
         }
     }
@@ -514,7 +522,7 @@ __device__ __forceinline__ void reduce_tail_block(const ReduceParams& p, int64_t
 // normally has one block per work item, so the hardware block scheduler hands
 // out the tiles in order as blocks retire; a grid-stride loop covers grids
 // capped below the item count.
-template <class T, int OP, int VB, bool MULTI>
+template <class T, int OP, int VB, int FORM>
 __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ ReduceParams p)
 {
     pdl_enter();
@@ -522,18 +530,26 @@ __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ 
     for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
         if (w < p.ntiles) {
             if constexpr (VB < 4) reduce_element_tile<T, OP>(p, w);
-            else reduce_vector_tile<T, OP, VB, MULTI>(p, w);
+            else reduce_vector_tile<T, OP, VB, FORM>(p, w);
         } else {
             if constexpr (VB >= 4) reduce_tail_block<T, OP, VB>(p, w - p.ntiles);
         }
     }
 }
 
+// The rank form follows the rank count; kWide runs on vectors of at most 8
+// bytes (the host narrows 16-byte vectors for 9 to 16 ranks).
 template <class T, int OP, int VB>
 cudaError_t launch_reduce_vb(const ReduceParams& p, dim3 grid, cudaStream_t s)
 {
-    if (VB >= 4 && p.nranks > kGroup) return launch_kernel(reduce_kernel<T, OP, VB, true>, grid, kBlock, 0, s, p);
-    return launch_kernel(reduce_kernel<T, OP, VB, false>, grid, kBlock, 0, s, p);
+    if constexpr (VB >= 4) {
+        if (p.nranks > 2 * kGroup) return launch_kernel(reduce_kernel<T, OP, VB, kGroups>, grid, kBlock, 0, s, p);
+        if (p.nranks > kGroup) {
+            if constexpr (VB == 16) return cudaErrorInvalidValue;
+            else return launch_kernel(reduce_kernel<T, OP, VB, kWide>, grid, kBlock, 0, s, p);
+        }
+    }
+    return launch_kernel(reduce_kernel<T, OP, VB, kOneGroup>, grid, kBlock, 0, s, p);
 }
 
 template <class T, int OP>
