@@ -192,6 +192,15 @@ template <>
 struct Pair16<__half> {
     using P = __half2;
     static __device__ __forceinline__ float2 widen(uint32_t w) { return __half22float2(bitcast<__half2>(w)); }
+    // lo += widen(low half of w), hi += widen(high half): Blackwell's
+    // mixed-precision add converts the 16-bit operand exactly to binary32 and
+    // adds with round-to-nearest-even, which is widen() then __fadd_rn.
+    static __device__ __forceinline__ void add_widened(float& lo, float& hi, uint32_t w)
+    {
+        asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; add.rn.f32.f16 %0, l, %0; add.rn.f32.f16 %1, h, %1; }"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w));
+    }
     static __device__ __forceinline__ uint32_t narrow(float lo, float hi)
     {
         return bitcast<uint32_t>(__floats2half2_rn(lo, hi));
@@ -209,6 +218,12 @@ template <>
 struct Pair16<__nv_bfloat16> {
     using P = __nv_bfloat162;
     static __device__ __forceinline__ float2 widen(uint32_t w) { return __bfloat1622float2(bitcast<__nv_bfloat162>(w)); }
+    static __device__ __forceinline__ void add_widened(float& lo, float& hi, uint32_t w)
+    {
+        asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; add.rn.f32.bf16 %0, l, %0; add.rn.f32.bf16 %1, h, %1; }"
+            : "+f"(lo), "+f"(hi)
+            : "r"(w));
+    }
     static __device__ __forceinline__ uint32_t narrow(float lo, float hi)
     {
         return bitcast<uint32_t>(__floats2bfloat162_rn(lo, hi));
@@ -239,13 +254,12 @@ struct Acc16Sum {
     {
 #pragma unroll
         for (int i = 0; i < W; ++i) {
-            const float2 f = Pair16<T>::widen(x.w[i]);
             if constexpr (OP == kProd) {
+                const float2 f = Pair16<T>::widen(x.w[i]);
                 a[2 * i] = __fmul_rn(a[2 * i], f.x);
                 a[2 * i + 1] = __fmul_rn(a[2 * i + 1], f.y);
             } else {
-                a[2 * i] = __fadd_rn(a[2 * i], f.x);
-                a[2 * i + 1] = __fadd_rn(a[2 * i + 1], f.y);
+                Pair16<T>::add_widened(a[2 * i], a[2 * i + 1], x.w[i]);
             }
         }
     }
