@@ -83,6 +83,8 @@ class Workload:
     dtype_compute = "f32"
     storage = ""
     kernel = ""
+    pipelined_e2e = False
+    e2e_inplace = False
     sources = REDUCE_SOURCES      # of the dominant kernel
 
     def config(self):
@@ -97,7 +99,7 @@ class TreduceBench(Workload):
     def __init__(self, w, storage):
         self.w, self.storage = w, storage
         self.name = w.name
-        self.kernel = "reduce_async_kernel<%s> (shared-memory pipeline)" % storage
+        self.kernel = "reduce_kernel<%s> (one block per tile)" % storage
         self.dtype_compute = "i32" if storage == "i32" else "f32"
 
     def bytes_per_launch(self):
@@ -173,7 +175,7 @@ class TreduceBench(Workload):
         w = self.w
         return {"workload": w.name, "op": "TREDUCE", "nranks": w.nranks, "storage_dtype": self.storage,
                 "shape": [w.rows, w.cols], "ld": w.ld, "valid": [w.valid_rows, w.valid_cols],
-                "ops": w.ops, "root": w.root, "values": "%s%s" % (w.dist[0], list(w.dist[1:])),
+                "ops": w.ops, "root": w.root, "values": ("normal(0,1)" if w.dist[0] == "normal" else "%s[%s, %s]" % w.dist),
                 "seed": "1234 + rank (SplitMix64, counter-based)",
                 "step": "%d TREDUCE launches (%s)" % (len(w.ops), ", ".join(w.ops)),
                 "bytes_per_step": self.bytes_per_step(),
@@ -237,7 +239,7 @@ class RsAgBench(Workload):
         self.name = "reduce_scatter_allgather_n8_f16_8192x4096"
         self.per_launch_timing = True
         self.storage = "f16"
-        self.kernel = "reduce_async_kernel<f16> (scatter mode) + gather_kernel"
+        self.kernel = "reduce_kernel<f16> (owner-window mode) + gather_kernel"
 
     def bytes_per_launch_list(self):
         c = self.cfg
@@ -274,19 +276,28 @@ class RsAgBench(Workload):
         else:
             P.ptoc_allgather(wins, c["rows"], c["cols"], c["ld"], P.F16)
 
+    # e2e: windows uploaded, reduced and gathered in place, read back
+    pipelined_e2e = True
+    e2e_inplace = True
+
     def setup_e2e(self, dev):
         import torch
         self.pinned = [_pin(h) for h in self.host]
-        self.out_pinned = [torch.empty(_nbytes(h), dtype=torch.uint8).pin_memory() for h in self.host]
-        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+        self.e2e_win = [[torch.empty_like(t) for t in self.dev] for _ in range(2)]
+        self.out_pinned = [_pinned_like(self.dev) for _ in range(2)]
 
-    def e2e_step(self):
-        for d, h in zip(self.e2e_dev, self.pinned):
-            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
-        self.launch(0, srcs=self.e2e_dev)
-        self.launch(1, srcs=self.e2e_dev)
-        for d, o in zip(self.e2e_dev, self.out_pinned):
-            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+    def e2e_upload(self, b):
+        _upload(self.e2e_win[b], self.pinned)
+
+    def e2e_compute(self, b):
+        self.launch(0, srcs=self.e2e_win[b])
+        self.launch(1, srcs=self.e2e_win[b])
+
+    def e2e_download(self, b):
+        _download(self.out_pinned[b], self.e2e_win[b])
+
+    def e2e_verify(self, b):
+        _check_same(self.out_pinned[b], self.dev, "window")
 
     def h2d_bytes(self):
         return sum(_nbytes(h) for h in self.host)
@@ -369,24 +380,44 @@ class A2avBench(Workload):
         P.ptoc_all_to_all_v(srcs or self.dev, self.d_tg, self.d_sc, self.d_rc, c["target_rows"], c["size"],
                             P.BF16)
 
+    # e2e: inputs and send counts uploaded, targets and recv counts read back;
+    # the targets start from the sentinel, so only rows the exchange wrote
+    # can match the resident run's
+    pipelined_e2e = True
+
     def setup_e2e(self, dev):
         import torch
-        self.pinned = [_pin(h) for h in self.host]
-        self.out_pinned = [torch.empty(_nbytes(h), dtype=torch.uint8).pin_memory() for h in self.host]
-        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        self.pinned = [_pin(h) for h in self.host] + [_pin(x) for x in self.sc]
+        self.e2e_in = [[torch.empty_like(t) for t in self.dev] + [torch.empty_like(t) for t in self.d_sc]
+                       for _ in range(2)]
+        self.e2e_out = [[torch.full((tr, size), -1, dtype=torch.int16, device=dev) for _ in range(n)] +
+                        [torch.zeros(n, dtype=torch.int32, device=dev) for _ in range(n)] for _ in range(2)]
+        self.out_pinned = [_pinned_like(self.e2e_out[0]) for _ in range(2)]
 
-    def e2e_step(self):
-        for d, h in zip(self.e2e_dev, self.pinned):
-            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
-        self.launch(0, srcs=self.e2e_dev)
-        for d, o in zip(self.d_tg, self.out_pinned):
-            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+    def e2e_upload(self, b):
+        _upload(self.e2e_in[b], self.pinned)
+
+    def e2e_compute(self, b):
+        import tile_level_collective_gb300 as P
+        c = self.cfg
+        n = c["nranks"]
+        P.ptoc_all_to_all_v(self.e2e_in[b][:n], self.e2e_out[b][:n], self.e2e_in[b][n:], self.e2e_out[b][n:],
+                            c["target_rows"], c["size"], P.BF16)
+
+    def e2e_download(self, b):
+        _download(self.out_pinned[b], self.e2e_out[b])
+
+    def e2e_verify(self, b):
+        _check_same(self.out_pinned[b], self.d_tg + self.d_rc, "target / recv_counts")
 
     def h2d_bytes(self):
-        return sum(_nbytes(h) for h in self.host)
+        return sum(_nbytes(h) for h in self.host) + sum(_nbytes(x) for x in self.sc)
 
     def d2h_bytes(self):
-        return sum(_nbytes(h) for h in self.host)
+        n = self.cfg["nranks"]
+        return sum(_nbytes(h) for h in self.host) + 4 * n * n
 
     def config(self):
         c = self.cfg
@@ -429,7 +460,7 @@ class WindowOpBench(Workload):
         self.cfg = synth.CONFIG4
         self.name = "%s_n8_f16_8192x4096" % op
         self.storage = "f16"
-        self.kernel = ("reduce_async_kernel<f16> (all-windows mode)" if op == "allreduce"
+        self.kernel = ("reduce_kernel<f16> (all-windows mode)" if op == "allreduce"
                        else "gather_kernel (fixed source window)")
         self.sources = REDUCE_SOURCES if op == "allreduce" else MOVE_SOURCES
         self.dtype_compute = "f32" if op == "allreduce" else "u16"
@@ -468,18 +499,27 @@ class WindowOpBench(Workload):
         else:
             P.ptoc_broadcast(wins, c["rows"], c["cols"], c["ld"], P.F16, root=0)
 
+    # e2e: windows uploaded, updated in place, read back
+    pipelined_e2e = True
+    e2e_inplace = True
+
     def setup_e2e(self, dev):
         import torch
         self.pinned = [_pin(h) for h in self.host]
-        self.out_pinned = [torch.empty(_nbytes(h), dtype=torch.uint8).pin_memory() for h in self.host]
-        self.e2e_dev = [torch.empty_like(t) for t in self.dev]
+        self.e2e_win = [[torch.empty_like(t) for t in self.dev] for _ in range(2)]
+        self.out_pinned = [_pinned_like(self.dev) for _ in range(2)]
 
-    def e2e_step(self):
-        for d, h in zip(self.e2e_dev, self.pinned):
-            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
-        self.launch(0, srcs=self.e2e_dev)
-        for d, o in zip(self.e2e_dev, self.out_pinned):
-            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+    def e2e_upload(self, b):
+        _upload(self.e2e_win[b], self.pinned)
+
+    def e2e_compute(self, b):
+        self.launch(0, srcs=self.e2e_win[b])
+
+    def e2e_download(self, b):
+        _download(self.out_pinned[b], self.e2e_win[b])
+
+    def e2e_verify(self, b):
+        _check_same(self.out_pinned[b], self.dev, "window")
 
     def h2d_bytes(self):
         return sum(_nbytes(h) for h in self.host)
@@ -526,6 +566,8 @@ class PairsBench(A2avBench):
         self.name = ("all_to_all_n16_bf16_7168_chunk1536" if op == "all_to_all"
                      else "all_to_all_v_combine_add_n16_bf16_7168_maxrecv1536")
         self.kernel = "pairs_kernel<CopyMover>" if op == "all_to_all" else "pairs_kernel<AddMover<bf16>>"
+        # the combine uploads into its outputs (kAdd reads them)
+        self.e2e_inplace = op == "combine"
         self.dtype_compute = "u16" if op == "all_to_all" else "f32"
 
     def setup_host(self):
@@ -538,9 +580,9 @@ class PairsBench(A2avBench):
             self.moved_rows = n * n * self.mr
         else:
             # dispatch values are normal bf16 (added, so they should be numbers)
-            self.host = [synth.values(("normal", 0, 0), synth.DT_BF16, 1234 + s, tr * size).reshape(tr, size)
+            self.host = [synth.values(("normal", 0, 1), synth.DT_BF16, 1234 + s, tr * size).reshape(tr, size)
                          for s in range(n)]
-            self.out_host = [synth.values(("normal", 0, 0), synth.DT_BF16, 5678 + s, tr * size).reshape(tr, size)
+            self.out_host = [synth.values(("normal", 0, 1), synth.DT_BF16, 5678 + s, tr * size).reshape(tr, size)
                              for s in range(n)]
 
     def bytes_per_launch(self):
@@ -576,19 +618,61 @@ class PairsBench(A2avBench):
             P.ptoc_all_to_all_v_combine(srcs or self.d_tg, self.d_out, self.d_rc, c["target_rows"], c["size"],
                                         P.ATOMIC_ADD, P.BF16)
 
+    # e2e, all_to_all: inputs uploaded, targets (from the sentinel) read back.
+    # combine: the dispatched windows, the recv counts and the outputs' prior
+    # contents (kAdd adds into them) uploaded, the outputs read back.
     def setup_e2e(self, dev):
         import torch
-        super().setup_e2e(dev)
-        if self.op == "combine":
-            self.pinned = [_pin(t.cpu().numpy()) for t in self.d_tg]
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        if self.op == "all_to_all":
+            self.pinned = [_pin(h) for h in self.host]
+            self.e2e_in = [[torch.empty_like(t) for t in self.dev] for _ in range(2)]
+            self.e2e_out = [[torch.full((tr, size), -1, dtype=torch.int16, device=dev) for _ in range(n)]
+                            for _ in range(2)]
+            self.e2e_ref = self.d_tg
+        else:
+            self.pinned = ([_pin(t.cpu().numpy()) for t in self.d_tg] + [_pin(t.cpu().numpy()) for t in self.d_rc] +
+                           [_pin(t.cpu().numpy()) for t in self.saved])
+            self.e2e_in = [[torch.empty_like(t) for t in self.d_tg] + [torch.empty_like(t) for t in self.d_rc]
+                           for _ in range(2)]
+            # the outputs are uploaded too (kAdd reads them), into the set's output buffers
+            self.e2e_out = [[torch.empty_like(t) for t in self.d_out] for _ in range(2)]
+            self.e2e_ref = self.d_out
+        self.out_pinned = [_pinned_like(self.e2e_out[0]) for _ in range(2)]
 
-    def e2e_step(self):
-        for d, h in zip(self.e2e_dev, self.pinned):
-            d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
-        self.launch(0, srcs=self.e2e_dev)
-        outs = self.d_tg if self.op == "all_to_all" else self.d_out
-        for d, o in zip(outs, self.out_pinned):
-            o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+    def e2e_upload(self, b):
+        if self.op == "all_to_all":
+            _upload(self.e2e_in[b], self.pinned)
+        else:
+            n = self.cfg["nranks"]
+            _upload(self.e2e_in[b], self.pinned[:2 * n])
+            _upload(self.e2e_out[b], self.pinned[2 * n:])
+
+    def e2e_compute(self, b):
+        import tile_level_collective_gb300 as P
+        c = self.cfg
+        n = c["nranks"]
+        if self.op == "all_to_all":
+            P.ptoc_all_to_all(self.e2e_in[b], self.e2e_out[b], c["target_rows"], c["size"], P.BF16)
+        else:
+            P.ptoc_all_to_all_v_combine(self.e2e_in[b][:n], self.e2e_out[b], self.e2e_in[b][n:], c["target_rows"],
+                                        c["size"], P.ATOMIC_ADD, P.BF16)
+
+    def e2e_download(self, b):
+        _download(self.out_pinned[b], self.e2e_out[b])
+
+    def e2e_verify(self, b):
+        _check_same(self.out_pinned[b], self.e2e_ref, "output")
+
+    def h2d_bytes(self):
+        if self.op == "all_to_all":
+            return sum(_nbytes(h) for h in self.host)
+        n = self.cfg["nranks"]
+        return sum(_nbytes(t) for t in self.d_tg) + 4 * n * n + sum(_nbytes(t) for t in self.saved)
+
+    def d2h_bytes(self):
+        return sum(_nbytes(t) for t in (self.d_tg if self.op == "all_to_all" else self.d_out))
 
     def config(self):
         c = dict(super().config())
@@ -722,6 +806,28 @@ def _to_dev(h, dev):
     h = np.ascontiguousarray(h)
     t = torch.from_numpy(h.view(np.int16) if h.dtype == np.uint16 else h)
     return t.to(dev)
+
+
+def _upload(dsts, pinned):
+    for d, h in zip(dsts, pinned):
+        d.view(-1).view(torch_uint8()).copy_(h, non_blocking=True)
+
+
+def _download(pinned, srcs):
+    for o, d in zip(pinned, srcs):
+        o.copy_(d.view(-1).view(torch_uint8()), non_blocking=True)
+
+
+def _pinned_like(ts):
+    import torch
+    return [torch.empty(_nbytes(t), dtype=torch.uint8).pin_memory() for t in ts]
+
+
+def _check_same(pinned, refs, what):
+    """The downloaded bytes equal the resident run's result tensors."""
+    for i, (o, d) in enumerate(zip(pinned, refs)):
+        if not bool((o == d.reshape(-1).view(torch_uint8()).cpu()).all()):
+            raise RuntimeError("pipelined end-to-end %s %d differs from the resident result" % (what, i))
 
 
 def _pin(h):
@@ -967,9 +1073,9 @@ def run_ours(args):
 def run_e2e_pipelined(wl, args, dev, world, barrier):
     """Steps of upload -> compute -> download on three streams with two
     buffer sets: step k's upload waits for step k-2's compute to release its
-    input set, its compute for its upload and for step k-2's download to
-    release its output set; the timed region spans the first upload to the
-    last download."""
+    input set (for in-place ops, for its download), its compute for its upload
+    and for step k-2's download to release its output set; the timed region
+    spans the first upload to the last download."""
     import torch
     wl.setup_e2e(dev)
     up, comp, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -982,7 +1088,9 @@ def run_e2e_pipelined(wl, args, dev, world, barrier):
             b = k & 1
             with torch.cuda.stream(up):
                 if used[b]:
-                    up.wait_event(computed[b])
+                    # the set's inputs are free once computed; in place, its
+                    # results must also have been read back
+                    up.wait_event(downloaded[b] if wl.e2e_inplace else computed[b])
                 wl.e2e_upload(b)
                 uploaded[b].record(up)
             with torch.cuda.stream(comp):
@@ -1014,23 +1122,9 @@ def run_e2e_pipelined(wl, args, dev, world, barrier):
 
 
 def run_e2e(wl, args, dev, stream, world, barrier):
-    import torch
-    if getattr(wl, "pipelined_e2e", False):
-        return run_e2e_pipelined(wl, args, dev, world, barrier)
-    wl.setup_e2e(dev)
-    for _ in range(max(1, min(args.warmup, 3))):
-        wl.e2e_step()
-    torch.cuda.synchronize()
-    e_steps = max(3, min(args.e2e_steps, args.steps))
-    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    es.record(stream)
-    for _ in range(e_steps):
-        wl.e2e_step()
-    ee.record(stream)
-    torch.cuda.synchronize()
-    return aggregate(es.elapsed_time(ee) / e_steps, wl.bytes_per_step(), world, dev)
+    if not wl.pipelined_e2e:
+        raise SystemExit("workload %s has no end-to-end leg" % wl.name)
+    return run_e2e_pipelined(wl, args, dev, world, barrier)
 
 
 def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl, clocks):
@@ -1048,9 +1142,9 @@ def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traff
             "value": round(e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": wl.h2d_bytes(),
             "d2h_bytes_per_step": wl.d2h_bytes(), "ms_per_step": round(e_ms, 6),
             "path": ("every step: pinned host -> device copy of its inputs, the library calls, device -> "
-                     "pinned host copy of its results" +
-                     ("; double-buffered on three streams (upload of step k overlaps compute and download "
-                      "of step k-1)" if getattr(wl, "pipelined_e2e", False) else ""))},
+                     "pinned host copy of its results; double-buffered on three streams (upload of step k "
+                     "overlaps compute and download of step k-1); the last results checked against the "
+                     "resident run")},
         "gpu_launches": nl * args.steps,
         "timing": ("CUDA events around each launch" if wl.per_launch_timing else
                    "CUDA events around each step; its %d launches run back to back (programmatic "

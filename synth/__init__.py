@@ -110,6 +110,8 @@ def values(dist, dtype, seed, n, start=0):
             return fill(UNIF_I32, seed, n, start, lo_i=lo, hi_i=hi)
         v = fill(UNIF_F32, seed, n, start, lo=lo, hi=hi)
     elif kind == "normal":
+        if (lo, hi) != (0, 1):
+            raise ValueError("only the standard normal N(0, 1) is generated")
         v = fill(NORM_F32, seed, n, start)
     else:
         raise ValueError(kind)
@@ -179,7 +181,7 @@ def config1():
 
 def config2():
     return TreduceWorkload("treduce_n8_bf16_4096x4096_valid4000", 8, DT_BF16, 4096, 4096, 4096,
-                           4000, 4000, ("normal", 0, 0), ["sum", "max", "min"],
+                           4000, 4000, ("normal", 0, 1), ["sum", "max", "min"],
                            src_pad=0x7FD5, dst_pad=0xFFD5)
 
 
@@ -193,7 +195,7 @@ def config3_int():
                            16384, 8192, ("uniform", -2**30, 2**30), ["max"])
 
 
-CONFIG4 = dict(nranks=8, rows=8192, cols=4096, ld=4096, dtype=DT_F16, dist=("normal", 0, 0))
+CONFIG4 = dict(nranks=8, rows=8192, cols=4096, ld=4096, dtype=DT_F16, dist=("normal", 0, 1))
 
 
 def window(r, cfg=CONFIG4):

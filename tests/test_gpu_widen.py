@@ -212,9 +212,9 @@ def test_dispatch_combine_full_size_bf16():
     hold other values; every output element against the oracle."""
     cfg = synth.CONFIG5
     n, tr, size = cfg["nranks"], cfg["target_rows"], cfg["size"]
-    inputs = [synth.values(("normal", 0, 0), synth.DT_BF16, 1234 + s, tr * size).reshape(tr, size)
+    inputs = [synth.values(("normal", 0, 1), synth.DT_BF16, 1234 + s, tr * size).reshape(tr, size)
               for s in range(n)]
-    outputs = [synth.values(("normal", 0, 0), synth.DT_BF16, 5678 + s, tr * size).reshape(tr, size)
+    outputs = [synth.values(("normal", 0, 1), synth.DT_BF16, 5678 + s, tr * size).reshape(tr, size)
                for s in range(n)]
     sc = [synth.a2av_send_counts(s, n) for s in range(n)]
     d_in = [to_dev(x) for x in inputs]

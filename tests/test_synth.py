@@ -64,7 +64,7 @@ def test_normal_moments():
 
 
 def test_workload_slices_and_samples():
-    w = synth.TreduceWorkload("t", 3, synth.DT_BF16, 7, 9, 12, 5, 8, ("normal", 0, 0),
+    w = synth.TreduceWorkload("t", 3, synth.DT_BF16, 7, 9, 12, 5, 8, ("normal", 0, 1),
                               ["sum"], src_pad=0x7FD5)
     s = w.slice(2)
     assert s.shape == (7, 12)
