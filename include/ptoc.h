@@ -19,8 +19,13 @@
  *     recv_counts) are HOST arrays of device pointers; they are read during
  *     the call and copied into kernel parameters, so the caller may free or
  *     reuse them as soon as the call returns.
- *   - The caller owns every buffer. The library allocates no device or host
- *     memory and keeps no per-call state.
+ *   - The caller owns every buffer. The library keeps no per-call state.
+ *     The only memory it takes is the 4-byte work counter of
+ *     ptoc_all_to_all_v and ptoc_all_to_all_v_combine: allocated in stream
+ *     order on `stream` (from a library-owned pool per device that never
+ *     returns its memory; from the default pool during stream capture, where
+ *     it becomes a graph memory node), zeroed, and freed in stream order
+ *     after the call's kernel. An allocation failure is PTOC_ERR_CUDA.
  *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
  *     stream). Completion is observed through the stream; results must not be
  *     read, and inputs must not be modified, before the stream reaches them.
@@ -193,6 +198,12 @@ ptoc_status ptoc_broadcast(const ptoc_group* windows,
  * inputs->nranks must equal targets->nranks; roots are ignored. Outputs
  * (targets, recv_counts) must not overlap each other or any input
  * (PTOC_ERR_ALIAS); inputs and send_counts may overlap one another.
+ * The counts are read on the device, so the work is scheduled there: one
+ * wave of blocks takes the moved tiles in order from a zeroed 4-byte counter
+ * (see the conventions above), and a sparse exchange costs in proportion to
+ * the rows it moves, not to the capacity of the windows. A call whose
+ * windows would hold 2^31 or more tiles (32 KiB each for 16-byte-aligned
+ * rows, less for narrower alignment) returns PTOC_ERR_UNSUPPORTED.
  */
 ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* targets,
                               const int32_t* const* send_counts, int32_t* const* recv_counts,
@@ -229,7 +240,8 @@ ptoc_status ptoc_all_to_all(const ptoc_group* inputs, const ptoc_group* targets,
  * floating types, wrapping for int32). Every output row has at most one
  * contributor, so the result does not depend on scheduling. Other output rows
  * are not written. Outputs must not overlap each other, the windows or the
- * counts (PTOC_ERR_ALIAS).
+ * counts (PTOC_ERR_ALIAS). Scheduled like ptoc_all_to_all_v (a 4-byte
+ * work counter per call).
  */
 ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, const ptoc_group* outputs,
                                       const int32_t* const* recv_counts,

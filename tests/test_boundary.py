@@ -180,3 +180,19 @@ def test_credit_barrier_rejects():
     assert B(sig, [0, 1], 1, 10 ** 9, sig[2] + 4, stream=0, check=False) == P.ERR_ALIAS  # status over a window
     assert P.ptoc_signal_reset([A, 0], stream=0, check=False) == P.ERR_INVALID_ARG
     assert P.ptoc_signal_reset([A + 2], stream=0, check=False) == P.ERR_INVALID_ARG
+
+
+def test_device_count_exchanges_reject_int32_tile_overflow():
+    """64 ranks, 8192-wide bf16 rows, MAX_RECV = 2^20: 4096 pairs x 2^19 tiles
+    of 32 KiB is past the int32 tile index of the claiming kernel, so the call
+    returns UNSUPPORTED before any CUDA call (fake, disjoint 1 TiB windows)."""
+    n, size, mr = 64, 8192, 1 << 20
+    tr_ = mr * n
+    B, S = 0x100000000000, 1 << 41
+    ins = [B + r * S for r in range(n)]
+    tgs = [B + (n + r) * S for r in range(n)]
+    sc = [B + 2 * n * S + 256 * r for r in range(n)]
+    rc = [B + 2 * n * S + (1 << 20) + 256 * r for r in range(n)]
+    assert P.ptoc_all_to_all_v(ins, tgs, sc, rc, tr_, size, P.BF16, stream=0, check=False) == P.ERR_UNSUPPORTED
+    assert P.ptoc_all_to_all_v_combine(ins, tgs, rc, tr_, size, P.ATOMIC_ADD, P.BF16, stream=0,
+                                       check=False) == P.ERR_UNSUPPORTED

@@ -14,13 +14,17 @@
 // combine (pld.tensor.put / remote_store with AtomicType kAdd) is the return
 // leg: rank d pushes the recv_counts[d][s] rows it holds from s back to s's
 // output, overwriting or adding. Because the rows of one pair are contiguous
-// on both sides, each pair is one contiguous copy of c * row_bytes bytes. The
-// counts live on the device, so the grid is sized for the largest possible
-// run: grid.y is the pair, grid.x the tile of the pair's run, one tile per
-// block. A block reads its pair's count (one L2-resident integer), publishes
-// it if it is the pair's first block, and exits at once when its tile lies
-// past the run; the hardware block scheduler hands out the live tiles in
-// order as blocks retire.
+// on both sides, each pair is one contiguous copy of c * row_bytes bytes.
+//
+// When every count is MAX_RECV (the symmetric all_to_all) the host knows the
+// tiles: grid.y is the pair, grid.x the tile of its run, one tile per block,
+// and the hardware block scheduler hands them out in order as blocks retire.
+// When the counts live on the device (all_to_all_v, the combine) a grid sized
+// for the largest runs would launch a block per possible tile, and empty
+// blocks cost about a nanosecond each: a sparse exchange would pay for its
+// capacity. So one wave of blocks is launched instead. Each block rebuilds the
+// pair counts and their tile prefix sums in shared memory, then claims the
+// live tiles one at a time, in order, from a counter that starts at zero.
 #include <cuda_runtime.h>
 
 #include "ptoc_internal.h"
@@ -100,6 +104,56 @@ __device__ __forceinline__ int32_t clamp_count(int32_t c, int64_t max_recv)
     return (int32_t)(v > max_recv ? max_recv : v);
 }
 
+// Per-pair state in shared memory: cnt[q] = clamped count of pair q
+// (q = a * N + b), pre[q] = tiles of pairs 0..q-1, pre[np] = all live tiles.
+// Each thread sums a contiguous run of pairs; the runs are combined with a
+// warp-shuffle scan and a pass over the warp totals. Block 0 also publishes
+// the counts when asked (all_to_all_v's recv_counts).
+__device__ void build_pairs(const A2avParams& p, int32_t* cnt, int32_t* pre, int32_t* warp_tot)
+{
+    const int n = p.nranks;
+    const int np = n * n;
+    const int per = (np + kBlock - 1) / kBlock;
+    const int q0 = threadIdx.x * per;
+    const int q1 = min(q0 + per, np);
+    int32_t run = 0;
+    for (int q = q0; q < q1; ++q) {
+        const int a = q / n, b = q - (q / n) * n;
+        const int32_t c = p.full ? (int32_t)p.max_recv : clamp_count(p.cnt[a][b], p.max_recv);
+        if (p.publish && blockIdx.x == 0) p.pub[b][a] = c;
+        cnt[q] = c;
+        const int32_t tiles = (int32_t)(((int64_t)c * p.row_bytes + p.tile_bytes - 1) / p.tile_bytes);
+        pre[q] = tiles;                 // this pair's tiles, until the scan below
+        run += tiles;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int32_t acc = 0;
+        for (int w = 0; w < kBlock / 32; ++w) {
+            const int32_t t = warp_tot[w];
+            warp_tot[w] = acc;
+            acc += t;
+        }
+        pre[np] = acc;
+    }
+    __syncthreads();
+    int32_t excl = warp_tot[warp] + incl - run;
+    for (int q = q0; q < q1; ++q) {
+        const int32_t tiles = pre[q];
+        pre[q] = excl;
+        excl += tiles;
+    }
+    __syncthreads();
+}
+
 // Moves one chunk of VB bytes: a copy, or (AddMover) out += in per element.
 template <int VB>
 struct CopyMover {
@@ -175,6 +229,57 @@ __global__ void __launch_bounds__(kBlock) pairs_kernel(const __grid_constant__ A
     }
 }
 
+// The same moves, claimed: tile t (counted over the live tiles of all pairs
+// in pair order) is pair q's tile t - pre[q], where pre[q] <= t < pre[q + 1].
+template <class M, int VB, int U>
+__global__ void __launch_bounds__(kBlock) pairs_claim_kernel(const __grid_constant__ A2avParams p)
+{
+    extern __shared__ int32_t smem[];
+    __shared__ int32_t warp_tot[kBlock / 32];
+    __shared__ int32_t claimed;
+    const int n = p.nranks;
+    const int np = n * n;
+    int32_t* cnt = smem;                    // np entries
+    int32_t* pre = smem + np;               // np + 1 entries
+    pdl_enter();
+    build_pairs(p, cnt, pre, warp_tot);
+    const int32_t total = pre[np];
+
+    while (true) {
+        if (threadIdx.x == 0) claimed = (int32_t)atomicAdd(p.claim, 1u);
+        __syncthreads();
+        const int32_t t = claimed;
+        __syncthreads();                    // all have read it before the next claim
+        if (t >= total) break;
+        int lo = 0, hi = np;                // invariant: pre[lo] <= t < pre[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= t) lo = mid;
+            else hi = mid;
+        }
+        const int q = lo;
+        const int a = q / n, b = q - (q / n) * n;
+        const int64_t bytes = (int64_t)cnt[q] * p.row_bytes;
+        const int64_t beg = (int64_t)(t - pre[q]) * p.tile_bytes;
+        const int64_t len = min(p.tile_bytes, bytes - beg);
+        const char* src = (const char*)p.in[a] + b * p.max_recv * p.row_bytes + beg;
+        char* dst = (char*)p.out[b] + a * p.max_recv * p.row_bytes + beg;
+        typename M::V x[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t o = ((int64_t)k * kBlock + threadIdx.x) * VB;
+            if (o < len) x[k] = M::load(src + o, dst + o);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t o = ((int64_t)k * kBlock + threadIdx.x) * VB;
+            if (o < len) M::store(dst + o, x[k]);
+        }
+    }
+}
+
+size_t pairs_claim_smem_bytes(int nranks) { return (size_t)(2 * nranks * nranks + 1) * sizeof(int32_t); }
+
 template <int U>
 static cudaError_t launch_a2av_u(const A2avParams& p, int vb, dim3 grid, cudaStream_t s)
 {
@@ -213,6 +318,92 @@ cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, 
     case PTOC_F16: return launch_add_t<__half>(p, vb, grid, s);
     default: return launch_add_t<__nv_bfloat16>(p, vb, grid, s);
     }
+}
+
+// ---- claiming launches --------------------------------------------------------
+
+template <class M, int VB, int U>
+static int claim_occupancy(size_t smem)
+{
+    int b = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, pairs_claim_kernel<M, VB, U>, kBlock, smem);
+    return (e == cudaSuccess && b > 0) ? b : 1;
+}
+
+template <class M, int VB, int U>
+static cudaError_t claim_launch(const A2avParams& p, int grid, size_t smem, cudaStream_t s)
+{
+    return launch_kernel(pairs_claim_kernel<M, VB, U>, dim3((unsigned)grid), kBlock, smem, s, p);
+}
+
+// The kernel family of one (add, dtype, vb, unroll): copies or kAdd adds.
+template <class F>
+static auto with_claim_kernel(bool add, int dtype, int vb, int unroll, F&& f)
+{
+    if (add) {
+        switch (dtype) {
+        case PTOC_F32:
+            if (vb == 16) return f.template go<AddMover<float, 16>, 16, kAddUnroll>();
+            if (vb == 8) return f.template go<AddMover<float, 8>, 8, kAddUnroll>();
+            return f.template go<AddMover<float, 4>, 4, kAddUnroll>();
+        case PTOC_I32:
+            if (vb == 16) return f.template go<AddMover<int32_t, 16>, 16, kAddUnroll>();
+            if (vb == 8) return f.template go<AddMover<int32_t, 8>, 8, kAddUnroll>();
+            return f.template go<AddMover<int32_t, 4>, 4, kAddUnroll>();
+        case PTOC_F16:
+            if (vb == 16) return f.template go<AddMover<__half, 16>, 16, kAddUnroll>();
+            if (vb == 8) return f.template go<AddMover<__half, 8>, 8, kAddUnroll>();
+            if (vb == 4) return f.template go<AddMover<__half, 4>, 4, kAddUnroll>();
+            return f.template go<AddMover1<__half>, 2, kAddUnroll>();
+        default:
+            if (vb == 16) return f.template go<AddMover<__nv_bfloat16, 16>, 16, kAddUnroll>();
+            if (vb == 8) return f.template go<AddMover<__nv_bfloat16, 8>, 8, kAddUnroll>();
+            if (vb == 4) return f.template go<AddMover<__nv_bfloat16, 4>, 4, kAddUnroll>();
+            return f.template go<AddMover1<__nv_bfloat16>, 2, kAddUnroll>();
+        }
+    }
+    if (unroll == 16) {
+        if (vb == 16) return f.template go<CopyMover<16>, 16, 16>();
+        if (vb == 8) return f.template go<CopyMover<8>, 8, 16>();
+        if (vb == 4) return f.template go<CopyMover<4>, 4, 16>();
+        return f.template go<CopyMover<2>, 2, 16>();
+    }
+    if (unroll == 4) {
+        if (vb == 16) return f.template go<CopyMover<16>, 16, 4>();
+        if (vb == 8) return f.template go<CopyMover<8>, 8, 4>();
+        if (vb == 4) return f.template go<CopyMover<4>, 4, 4>();
+        return f.template go<CopyMover<2>, 2, 4>();
+    }
+    if (vb == 16) return f.template go<CopyMover<16>, 16, 8>();
+    if (vb == 8) return f.template go<CopyMover<8>, 8, 8>();
+    if (vb == 4) return f.template go<CopyMover<4>, 4, 8>();
+    return f.template go<CopyMover<2>, 2, 8>();
+}
+
+struct ClaimOccupancy {
+    size_t smem;
+    template <class M, int VB, int U>
+    int go() const { return claim_occupancy<M, VB, U>(smem); }
+};
+
+struct ClaimLaunch {
+    const A2avParams& p;
+    int grid;
+    size_t smem;
+    cudaStream_t s;
+    template <class M, int VB, int U>
+    cudaError_t go() const { return claim_launch<M, VB, U>(p, grid, smem, s); }
+};
+
+int pairs_claim_blocks_per_sm(bool add, int dtype, int vb, int unroll, int nranks)
+{
+    return with_claim_kernel(add, dtype, vb, unroll, ClaimOccupancy{pairs_claim_smem_bytes(nranks)});
+}
+
+cudaError_t launch_pairs_claim(const A2avParams& p, bool add, int dtype, int vb, int unroll, int grid,
+                               cudaStream_t s)
+{
+    return with_claim_kernel(add, dtype, vb, unroll, ClaimLaunch{p, grid, pairs_claim_smem_bytes(p.nranks), s});
 }
 
 }  // namespace ptoc

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -96,6 +97,58 @@ int sm_count()
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 1;
     if (dev < kMaxDevices) g_sm_count[dev].store(c, std::memory_order_relaxed);
     return c;
+}
+
+// The 4-byte tile counters of the claiming exchanges come from one small
+// memory pool per device, created on first use, that never returns its memory
+// to the driver: it only ever holds the counters of calls in flight (one
+// granule). A pool that releases at synchronization (the default pool does)
+// would have to map memory again on the next call, which measured ~100 us of
+// host time. During stream capture the default pool is used, so that the
+// allocation becomes a graph memory node.
+std::atomic<cudaMemPool_t> g_scratch_pool[kMaxDevices];
+std::mutex g_scratch_pool_mu;
+
+cudaMemPool_t scratch_pool(int dev)
+{
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    cudaMemPool_t pool = g_scratch_pool[dev].load(std::memory_order_acquire);
+    if (pool) return pool;
+    std::lock_guard<std::mutex> lock(g_scratch_pool_mu);
+    pool = g_scratch_pool[dev].load(std::memory_order_relaxed);
+    if (pool) return pool;
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = ~(uint64_t)0;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    g_scratch_pool[dev].store(pool, std::memory_order_release);
+    return pool;
+}
+
+// A zeroed 4-byte counter in stream order on `stream`, or nullptr.
+uint32_t* zeroed_counter(cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return nullptr;
+    void* ptr = nullptr;
+    cudaError_t e;
+    if (cap == cudaStreamCaptureStatusActive) {
+        e = cudaMallocAsync(&ptr, sizeof(uint32_t), stream);
+    } else {
+        cudaMemPool_t pool = scratch_pool(current_device());
+        if (!pool) return nullptr;
+        e = cudaMallocFromPoolAsync(&ptr, sizeof(uint32_t), pool, stream);
+    }
+    if (e != cudaSuccess) return nullptr;
+    if (cudaMemsetAsync(ptr, 0, sizeof(uint32_t), stream) != cudaSuccess) {
+        cudaFreeAsync(ptr, stream);
+        return nullptr;
+    }
+    return (uint32_t*)ptr;
 }
 
 // Chunks per thread per all_to_all_v tile: PTOC_A2AV_UNROLL=4|8|16 (A/B
@@ -238,15 +291,27 @@ ptoc_status launch_pairs(A2avParams& p, const void* const* a, const void* const*
     const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
     const int unroll = add ? 4 : a2av_unroll();
     p.tile_bytes = (int64_t)vb * kBlock * unroll;
-    // grid.y = the N^2 pairs, grid.x = the tiles of the longest possible run
-    // (MAX_RECV rows); blocks past their pair's run exit at once
-    const int64_t run = p.max_recv * p.row_bytes;
-    int64_t gx = (run + p.tile_bytes - 1) / p.tile_bytes;
-    const int64_t cap = (int64_t)1 << 30;
-    gx = gx < 1 ? 1 : (gx > cap ? cap : gx);
-    const dim3 grid((unsigned)gx, (unsigned)(n * n));
-    const cudaError_t e = add ? launch_pairs_add(p, dtype, vb, grid, stream) : launch_a2av(p, vb, unroll, grid, stream);
-    return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+    const int64_t run = p.max_recv * p.row_bytes;   // bytes of the longest possible run
+    const int64_t run_tiles = (run + p.tile_bytes - 1) / p.tile_bytes;
+    if (p.full) {
+        // every count is MAX_RECV: grid.y = the N^2 pairs, grid.x = the tiles of a run
+        const int64_t cap = (int64_t)1 << 30;
+        const int64_t gx = run_tiles < 1 ? 1 : (run_tiles > cap ? cap : run_tiles);
+        const dim3 grid((unsigned)gx, (unsigned)(n * n));
+        const cudaError_t e = add ? launch_pairs_add(p, dtype, vb, grid, stream) : launch_a2av(p, vb, unroll, grid, stream);
+        return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+    }
+    // counts on the device: one wave of blocks claims the live tiles from a
+    // zeroed counter (a 4-byte stream-ordered allocation, freed in stream
+    // order after the launch); tile indices are int32 in the kernel
+    if ((int64_t)n * n * (run_tiles + 1) >= INT32_MAX) return PTOC_ERR_UNSUPPORTED;
+    const int grid = sm_count() * pairs_claim_blocks_per_sm(add, dtype, vb, unroll, n);
+    uint32_t* claim = zeroed_counter(stream);
+    if (!claim) return PTOC_ERR_CUDA;
+    p.claim = claim;
+    const cudaError_t e = launch_pairs_claim(p, add, dtype, vb, unroll, grid, stream);
+    const cudaError_t f = cudaFreeAsync(claim, stream);
+    return (e == cudaSuccess && f == cudaSuccess) ? PTOC_OK : PTOC_ERR_CUDA;
 }
 
 ptoc_status check_pair_group(const ptoc_group* a, const ptoc_group* b)

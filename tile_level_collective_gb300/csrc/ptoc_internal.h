@@ -56,8 +56,10 @@ struct GatherParams {
 //   combine      : a = the rank that received, b = the original sender,
 //                  count = clamp(cnt[a][b]) with cnt = recv_counts; out is
 //                  overwritten or added into (AtomicType).
-// Each pair is one contiguous segment cut into tiles of tile_bytes; block
-// (x, q) of the launch moves tile x of pair q and reads only q's count.
+// Each pair is one contiguous segment cut into tiles of tile_bytes. With every
+// count known (full), block (x, q) of a 2-D launch moves tile x of pair q.
+// With counts on the device, a persistent grid claims the live tiles in order
+// from the counter at `claim`.
 struct A2avParams {
     const void* in[kMaxRanks];
     void* out[kMaxRanks];
@@ -66,6 +68,7 @@ struct A2avParams {
     int64_t max_recv;             // target_rows / nranks
     int64_t row_bytes;            // size * element bytes
     int64_t tile_bytes;           // bytes one block moves (the last tile of a run is shorter)
+    uint32_t* claim;              // tile counter of the claiming kernel (zeroed before the launch)
     int32_t nranks;
     int32_t full;                 // 1: every count is MAX_RECV
     int32_t publish;              // 1: write pub[b][a]
@@ -101,6 +104,11 @@ cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, dim3 grid, 
 cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s);
+// Claiming launches (counts on the device): blocks per SM, and the launch
+// with its dynamic shared memory (the pair counts and tile prefix sums).
+int pairs_claim_blocks_per_sm(bool add, int dtype, int vb, int unroll, int nranks);
+cudaError_t launch_pairs_claim(const A2avParams& p, bool add, int dtype, int vb, int unroll, int grid,
+                               cudaStream_t s);
 // The combine with AtomicType kAdd: out += in per element (binary32 for
 // floating types, one RNE narrowing; int32 wraps).
 cudaError_t launch_pairs_add(const A2avParams& p, int dtype, int vb, dim3 grid, cudaStream_t s);
