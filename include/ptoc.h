@@ -211,6 +211,25 @@ ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* target
                               cudaStream_t stream);
 
 /*
+ * ptoc_all_to_all_v_noalloc - ptoc_all_to_all_v without any allocation. The
+ * pages have no counterpart of this entry point: it serves callers that may
+ * not allocate during a call, at the price of one exchange in flight at a time.
+ * Arguments, results, checks and errors are those of ptoc_all_to_all_v. Its
+ * only scratch is a 4-byte tile counter taken from a fixed 256-byte block of
+ * device memory inside the library (its address is looked up once per device).
+ * Each call zeroes the counter with a stream-ordered memset; no call allocates
+ * or frees memory. A call whose scratch would not fit in the block returns
+ * PTOC_ERR_UNSUPPORTED (the counter always fits).
+ * Calls whose kernels can overlap (on different streams, from different
+ * threads, or through graph replays) share the counter and RACE: their
+ * results are undefined. Serialize them, for instance on one stream.
+ */
+ptoc_status ptoc_all_to_all_v_noalloc(const ptoc_group* inputs, const ptoc_group* targets,
+                                      const int32_t* const* send_counts, int32_t* const* recv_counts,
+                                      int64_t target_rows, int64_t size, ptoc_dtype dtype,
+                                      cudaStream_t stream);
+
+/*
  * ptoc_all_to_all - symmetric all-to-all ([DO] op table: every rank pushes
  * its per-destination chunks to every peer's window; the window is the
  * result). Layout as ptoc_all_to_all_v with C = target_rows / N rows per

@@ -67,6 +67,7 @@ _lib.ptoc_reduce_scatter.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, ctypes.
 _lib.ptoc_allgather.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, _vp]
 _lib.ptoc_all_to_all_v.argtypes = [_G, _G, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i64, _i64,
                                    ctypes.c_int, _vp]
+_lib.ptoc_all_to_all_v_noalloc.argtypes = _lib.ptoc_all_to_all_v.argtypes
 _lib.ptoc_allreduce.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp]
 _lib.ptoc_broadcast.argtypes = [_G, _i64, _i64, _i64, ctypes.c_int, _vp]
 _lib.ptoc_all_to_all.argtypes = [_G, _G, _i64, _i64, ctypes.c_int, _vp]
@@ -75,7 +76,7 @@ _lib.ptoc_all_to_all_v_combine.argtypes = [_G, _G, ctypes.POINTER(_vp), _i64, _i
 _lib.ptoc_credit_barrier.argtypes = [_G, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                      _i64, _vp, _vp]
 _lib.ptoc_signal_reset.argtypes = [_G, _vp]
-for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v",
+for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v", "ptoc_all_to_all_v_noalloc",
            "ptoc_allreduce", "ptoc_broadcast", "ptoc_all_to_all", "ptoc_all_to_all_v_combine",
            "ptoc_credit_barrier", "ptoc_signal_reset"):
     getattr(_lib, _f).restype = ctypes.c_int
@@ -157,6 +158,17 @@ def ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows, si
     st = _lib.ptoc_all_to_all_v(ctypes.byref(gi), ctypes.byref(gt), sc, rc, target_rows, size,
                                 int(dtype), _stream(stream))
     return _done(st, "ptoc_all_to_all_v", check)
+
+
+def ptoc_all_to_all_v_noalloc(inputs, targets, send_counts, recv_counts, target_rows, size, dtype,
+                              stream=None, check=True):
+    gi, k1 = _group(inputs)
+    gt, k2 = _group(targets)
+    sc = _ptr_array(send_counts)
+    rc = _ptr_array(recv_counts)
+    st = _lib.ptoc_all_to_all_v_noalloc(ctypes.byref(gi), ctypes.byref(gt), sc, rc, target_rows, size,
+                                        int(dtype), _stream(stream))
+    return _done(st, "ptoc_all_to_all_v_noalloc", check)
 
 
 def ptoc_allreduce(windows, rows, cols, ld, op, dtype, stream=None, check=True):

@@ -283,33 +283,58 @@ ptoc_status check_disjoint_outputs(const Span* writes, int nw, const Span* reads
 
 // The vector width and tile size of a pairwise exchange, and its launch.
 // `add` selects the combine's add mover (needs the element type).
-ptoc_status launch_pairs(A2avParams& p, const void* const* a, const void* const* b, int n, int eb, int dtype,
-                         bool add, cudaStream_t stream)
+// Vector width and tile of an exchange (sets p.tile_bytes).
+struct PairsPlan {
+    int vb, unroll;
+    int64_t run_tiles;   // tiles of the longest possible run (MAX_RECV rows)
+};
+
+PairsPlan plan_pairs(A2avParams& p, const void* const* a, const void* const* b, int n, int eb, bool add)
 {
     uintptr_t addr_or = 0;
     for (int r = 0; r < n; ++r) addr_or |= (uintptr_t)a[r] | (uintptr_t)b[r];
-    const int vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
-    const int unroll = add ? 4 : a2av_unroll();
-    p.tile_bytes = (int64_t)vb * kBlock * unroll;
-    const int64_t run = p.max_recv * p.row_bytes;   // bytes of the longest possible run
-    const int64_t run_tiles = (run + p.tile_bytes - 1) / p.tile_bytes;
+    PairsPlan pl;
+    pl.vb = pick_vector_bytes(addr_or, p.row_bytes, eb);
+    pl.unroll = add ? 4 : a2av_unroll();
+    p.tile_bytes = (int64_t)pl.vb * kBlock * pl.unroll;
+    const int64_t run = p.max_recv * p.row_bytes;
+    pl.run_tiles = (run + p.tile_bytes - 1) / p.tile_bytes;
+    return pl;
+}
+
+// Tile indices are int32 in the claiming kernel.
+bool claim_fits(int n, const PairsPlan& pl) { return (int64_t)n * n * (pl.run_tiles + 1) < INT32_MAX; }
+
+// One wave of blocks claiming the live tiles from `counter`, which the
+// stream has zeroed before this launch.
+cudaError_t launch_claimed(A2avParams& p, const PairsPlan& pl, int n, int dtype, bool add, uint32_t* counter,
+                           cudaStream_t stream)
+{
+    const int grid = sm_count() * pairs_claim_blocks_per_sm(add, dtype, pl.vb, pl.unroll, n);
+    p.claim = counter;
+    return launch_pairs_claim(p, add, dtype, pl.vb, pl.unroll, grid, stream);
+}
+
+ptoc_status launch_pairs(A2avParams& p, const void* const* a, const void* const* b, int n, int eb, int dtype,
+                         bool add, cudaStream_t stream)
+{
+    const PairsPlan pl = plan_pairs(p, a, b, n, eb, add);
     if (p.full) {
         // every count is MAX_RECV: grid.y = the N^2 pairs, grid.x = the tiles of a run
         const int64_t cap = (int64_t)1 << 30;
-        const int64_t gx = run_tiles < 1 ? 1 : (run_tiles > cap ? cap : run_tiles);
+        const int64_t gx = pl.run_tiles < 1 ? 1 : (pl.run_tiles > cap ? cap : pl.run_tiles);
         const dim3 grid((unsigned)gx, (unsigned)(n * n));
-        const cudaError_t e = add ? launch_pairs_add(p, dtype, vb, grid, stream) : launch_a2av(p, vb, unroll, grid, stream);
+        const cudaError_t e = add ? launch_pairs_add(p, dtype, pl.vb, grid, stream)
+                                  : launch_a2av(p, pl.vb, pl.unroll, grid, stream);
         return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
     }
     // counts on the device: one wave of blocks claims the live tiles from a
     // zeroed counter (a 4-byte stream-ordered allocation, freed in stream
-    // order after the launch); tile indices are int32 in the kernel
-    if ((int64_t)n * n * (run_tiles + 1) >= INT32_MAX) return PTOC_ERR_UNSUPPORTED;
-    const int grid = sm_count() * pairs_claim_blocks_per_sm(add, dtype, vb, unroll, n);
+    // order after the launch)
+    if (!claim_fits(n, pl)) return PTOC_ERR_UNSUPPORTED;
     uint32_t* claim = zeroed_counter(stream);
     if (!claim) return PTOC_ERR_CUDA;
-    p.claim = claim;
-    const cudaError_t e = launch_pairs_claim(p, add, dtype, vb, unroll, grid, stream);
+    const cudaError_t e = launch_claimed(p, pl, n, dtype, add, claim, stream);
     const cudaError_t f = cudaFreeAsync(claim, stream);
     return (e == cudaSuccess && f == cudaSuccess) ? PTOC_OK : PTOC_ERR_CUDA;
 }
@@ -488,10 +513,10 @@ extern "C" ptoc_status ptoc_broadcast(const ptoc_group* windows, int64_t rows, i
     return window_copy(windows, rows, cols, ld, dtype, stream, windows->root);
 }
 
-extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* targets,
-                                         const int32_t* const* send_counts, int32_t* const* recv_counts,
-                                         int64_t target_rows, int64_t size, ptoc_dtype dtype,
-                                         cudaStream_t stream)
+// Checks and kernel parameters of an all_to_all_v call (no CUDA call).
+static ptoc_status a2av_setup(const ptoc_group* inputs, const ptoc_group* targets,
+                              const int32_t* const* send_counts, int32_t* const* recv_counts,
+                              int64_t target_rows, int64_t size, ptoc_dtype dtype, A2avParams& p, int& eb)
 {
     ptoc_status st = check_pair_group(inputs, targets);
     if (st != PTOC_OK) return st;
@@ -499,7 +524,7 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
     if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
     if (target_rows < 0 || size < 0) return PTOC_ERR_INVALID_ARG;
     const int n = inputs->nranks;
-    const int eb = elem_size(dtype);
+    eb = elem_size(dtype);
     const int64_t fp = footprint(target_rows, size, size, eb);
     if (fp < 0) return PTOC_ERR_INVALID_ARG;
     for (int r = 0; r < n; ++r) {
@@ -520,7 +545,6 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
     st = check_disjoint_outputs(writes, 2 * n, reads, 2 * n);
     if (st != PTOC_OK) return st;
 
-    A2avParams p;
     memset(&p, 0, sizeof(p));
     for (int r = 0; r < n; ++r) {
         p.in[r] = inputs->tensors[r];
@@ -533,7 +557,64 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
     p.row_bytes = size * eb;
     p.full = 0;
     p.publish = 1;
-    return launch_pairs(p, inputs->tensors, targets->tensors, n, eb, dtype, false, stream);
+    return PTOC_OK;
+}
+
+extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_group* targets,
+                                         const int32_t* const* send_counts, int32_t* const* recv_counts,
+                                         int64_t target_rows, int64_t size, ptoc_dtype dtype,
+                                         cudaStream_t stream)
+{
+    A2avParams p;
+    int eb = 0;
+    const ptoc_status st = a2av_setup(inputs, targets, send_counts, recv_counts, target_rows, size, dtype, p, eb);
+    if (st != PTOC_OK) return st;
+    return launch_pairs(p, inputs->tensors, targets->tensors, inputs->nranks, eb, dtype, false, stream);
+}
+
+// ---- all_to_all_v without allocation ------------------------------------------
+
+// The scratch of ptoc_all_to_all_v_noalloc: a fixed 256-byte block of device
+// memory in the library image (zero at load). A call needs one 4-byte tile
+// counter from it; calls in flight at the same time share it and race.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
+
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+// The scratch block's device address on the current device, looked up once
+// per device (with that device current).
+static uint32_t* noalloc_scratch()
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    void* a = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return nullptr;
+        g_noalloc_addr[dev].store(a, std::memory_order_release);
+    }
+    return (uint32_t*)a;
+}
+
+extern "C" ptoc_status ptoc_all_to_all_v_noalloc(const ptoc_group* inputs, const ptoc_group* targets,
+                                                 const int32_t* const* send_counts, int32_t* const* recv_counts,
+                                                 int64_t target_rows, int64_t size, ptoc_dtype dtype,
+                                                 cudaStream_t stream)
+{
+    A2avParams p;
+    int eb = 0;
+    const ptoc_status st = a2av_setup(inputs, targets, send_counts, recv_counts, target_rows, size, dtype, p, eb);
+    if (st != PTOC_OK) return st;
+    const int n = inputs->nranks;
+    const PairsPlan pl = plan_pairs(p, inputs->tensors, targets->tensors, n, eb, false);
+    if (!claim_fits(n, pl)) return PTOC_ERR_UNSUPPORTED;
+    const size_t need = sizeof(uint32_t);        // the tile counter
+    if (need > kNoAllocScratchBytes) return PTOC_ERR_UNSUPPORTED;
+    uint32_t* counter = noalloc_scratch();
+    if (!counter) return PTOC_ERR_CUDA;
+    // the counter must start at zero for every call
+    if (cudaMemsetAsync(counter, 0, need, stream) != cudaSuccess) return PTOC_ERR_CUDA;
+    return launch_claimed(p, pl, n, dtype, false, counter, stream) == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
 }
 
 extern "C" ptoc_status ptoc_all_to_all(const ptoc_group* inputs, const ptoc_group* targets,
