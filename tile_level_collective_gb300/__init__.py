@@ -253,10 +253,12 @@ def allgather(windows, stream=None):
     return ptoc_allgather(windows, rows, cols, ld, dtype_code(windows[0]), stream=stream)
 
 
-def all_to_all_v(inputs, targets, send_counts, recv_counts, stream=None):
+def all_to_all_v(inputs, targets, send_counts, recv_counts, stream=None, noalloc=False):
+    """noalloc=True: ptoc_all_to_all_v_noalloc (no allocation; one call in
+    flight at a time)."""
     tr, size = targets[0].shape
-    return ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, tr, size,
-                             dtype_code(targets[0]), stream=stream)
+    f = ptoc_all_to_all_v_noalloc if noalloc else ptoc_all_to_all_v
+    return f(inputs, targets, send_counts, recv_counts, tr, size, dtype_code(targets[0]), stream=stream)
 
 
 def allreduce(windows, op="sum", stream=None):

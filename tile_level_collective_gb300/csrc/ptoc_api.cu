@@ -136,13 +136,9 @@ uint32_t* zeroed_counter(cudaStream_t stream)
     if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return nullptr;
     void* ptr = nullptr;
     cudaError_t e;
-    if (cap == cudaStreamCaptureStatusActive) {
-        e = cudaMallocAsync(&ptr, sizeof(uint32_t), stream);
-    } else {
-        cudaMemPool_t pool = scratch_pool(current_device());
-        if (!pool) return nullptr;
-        e = cudaMallocFromPoolAsync(&ptr, sizeof(uint32_t), pool, stream);
-    }
+    cudaMemPool_t pool = cap == cudaStreamCaptureStatusActive ? nullptr : scratch_pool(current_device());
+    if (pool) e = cudaMallocFromPoolAsync(&ptr, sizeof(uint32_t), pool, stream);
+    else e = cudaMallocAsync(&ptr, sizeof(uint32_t), stream);   // capture, or no pool of our own
     if (e != cudaSuccess) return nullptr;
     if (cudaMemsetAsync(ptr, 0, sizeof(uint32_t), stream) != cudaSuccess) {
         cudaFreeAsync(ptr, stream);
