@@ -333,14 +333,18 @@ class RsAgBench(Workload):
 
 
 class A2avBench(Workload):
-    """all_to_all_v: 16 ranks, bf16 rows of 7168, target_rows 24576."""
+    """all_to_all_v: 16 ranks, bf16 rows of 7168, target_rows 24576. With
+    count_div > 1 every send count is divided by it (a sparse exchange on the
+    same windows: 64 gives about 1 % of the capacity)."""
 
-    def __init__(self):
+    def __init__(self, count_div=1):
         import synth
         self.cfg = synth.CONFIG5
-        self.name = "all_to_all_v_n16_bf16_7168_maxrecv1536"
+        self.count_div = count_div
+        self.name = ("all_to_all_v_n16_bf16_7168_maxrecv1536" if count_div == 1 else
+                     "all_to_all_v_sparse_n16_bf16_7168_maxrecv1536_counts_div%d" % count_div)
         self.storage = "bf16"
-        self.kernel = "pairs_kernel<CopyMover>"
+        self.kernel = "pairs_claim_kernel<CopyMover>"
         self.dtype_compute = "u16"
         self.sources = MOVE_SOURCES
 
@@ -351,7 +355,7 @@ class A2avBench(Workload):
         n, tr, size = c["nranks"], c["target_rows"], c["size"]
         self.mr = tr // n
         self.host = [synth.a2av_input(s, n, tr, size) for s in range(n)]
-        self.sc = [synth.a2av_send_counts(s, n) for s in range(n)]
+        self.sc = [synth.a2av_send_counts(s, n) // self.count_div for s in range(n)]
         moved = sum(int(np.clip(c_, 0, self.mr).sum()) for c_ in self.sc)
         self.moved_rows = moved
 
@@ -423,7 +427,8 @@ class A2avBench(Workload):
         c = self.cfg
         return {"workload": self.name, "op": "all_to_all_v", "nranks": c["nranks"], "storage_dtype": "bf16",
                 "row_elems": c["size"], "target_rows": c["target_rows"], "max_recv": self.mr,
-                "send_counts": "uniform int [0, 2047] per (src, dest), seed 1234 + src",
+                "send_counts": "uniform int [0, 2047] per (src, dest), seed 1234 + src" +
+                               ("" if self.count_div == 1 else ", divided by %d" % self.count_div),
                 "moved_rows": self.moved_rows, "bytes_per_step": self.bytes_per_step(),
                 "l2": L2_NOTE}
 
@@ -565,7 +570,7 @@ class PairsBench(A2avBench):
         self.op = op
         self.name = ("all_to_all_n16_bf16_7168_chunk1536" if op == "all_to_all"
                      else "all_to_all_v_combine_add_n16_bf16_7168_maxrecv1536")
-        self.kernel = "pairs_kernel<CopyMover>" if op == "all_to_all" else "pairs_kernel<AddMover<bf16>>"
+        self.kernel = "pairs_kernel<CopyMover>" if op == "all_to_all" else "pairs_claim_kernel<AddMover<bf16>>"
         # the combine uploads into its outputs (kAdd reads them)
         self.e2e_inplace = op == "combine"
         self.dtype_compute = "u16" if op == "all_to_all" else "f32"
@@ -765,6 +770,8 @@ def make_workload(name, rows_div=1):
         wl = RsAgBench()
     elif name == "a2av":
         wl = A2avBench()
+    elif name == "a2av_sparse":
+        wl = A2avBench(count_div=64)
     elif name in ("allreduce", "broadcast"):
         wl = WindowOpBench(name)
     elif name in ("all_to_all", "combine"):
@@ -1197,7 +1204,8 @@ def parse(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="treduce",
                     choices=["treduce", "treduce_bf16", "treduce_small", "treduce_f32", "treduce_i32",
-                             "rs_ag", "a2av", "allreduce", "broadcast", "all_to_all", "combine", "barrier"])
+                             "rs_ag", "a2av", "a2av_sparse", "allreduce", "broadcast", "all_to_all", "combine",
+                             "barrier"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
