@@ -43,6 +43,7 @@ __device__ __forceinline__ int32_t credit_load(const int32_t* cell)
 }
 
 constexpr uint32_t kMaxPolls = 1u << 24;   // iteration cap behind the deadline
+constexpr uint32_t kSpinPolls = 64;        // polls before the nanosleep back-off starts
 
 __global__ void __launch_bounds__(32) credit_barrier_kernel(const __grid_constant__ BarrierParams p)
 {
@@ -69,8 +70,10 @@ __global__ void __launch_bounds__(32) credit_barrier_kernel(const __grid_constan
                 status = g;
                 break;
             }
-            __nanosleep(pause);
-            if (pause < 1024) pause <<= 1;
+            if (polls > kSpinPolls) {
+                __nanosleep(pause);
+                if (pause < 1024) pause <<= 1;
+            }
         }
     }
     if (status == 0)
