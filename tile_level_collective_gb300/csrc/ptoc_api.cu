@@ -253,9 +253,9 @@ ptoc_status check_windows(const ptoc_group* w, int64_t rows, int64_t cols, int64
 }
 
 // Shared checks of the pairwise exchanges over [target_rows, size] buffers
-// (all_to_all_v, all_to_all, the combine). `writes` are the buffers the call
-// writes (each `wbytes` long), `reads` the ones it only reads; outputs must not
-// overlap anything, inputs may overlap each other.
+// (all_to_all_v, all_to_all, the combine). `writes` are the spans the call
+// writes, `reads` the ones it only reads; outputs must not overlap anything,
+// inputs may overlap each other.
 struct Span {
     const void* p;
     uintptr_t bytes;
@@ -277,9 +277,8 @@ ptoc_status check_disjoint_outputs(const Span* writes, int nw, const Span* reads
     return PTOC_OK;
 }
 
-// The vector width and tile size of a pairwise exchange, and its launch.
-// `add` selects the combine's add mover (needs the element type).
-// Vector width and tile of an exchange (sets p.tile_bytes).
+// Vector width and tile of a pairwise exchange (sets p.tile_bytes); `add`
+// selects the combine's add mover, which moves 4 chunks per thread.
 struct PairsPlan {
     int vb, unroll;
     int64_t run_tiles;   // tiles of the longest possible run (MAX_RECV rows)
