@@ -62,3 +62,35 @@ def test_more_than_2_31_elements(layout):
             assert np.all(dst[torch.from_numpy(pad_k).cuda()].cpu().numpy() == 7)
     del srcs, dst
     torch.cuda.empty_cache()
+
+
+def test_all_to_all_v_runs_past_2_gib():
+    """2 ranks of 32 KiB rows, MAX_RECV 80,000: each full pair run is 2.6 GB,
+    so byte offsets inside a run pass 2^31. The exchange is a bit copy, so the
+    expected target rows are the definition itself: target d row s*MR + i is
+    input s row d*MR + i for i < the clamped count, and untouched rows keep
+    their fill. Checked on sampled rows, every run's first and last row, and
+    the first row past each run."""
+    n, size, mr = 2, 8192, 80_000                  # int32 elements: 32 KiB rows
+    tr = n * mr
+    counts = np.array([[mr, mr - 1], [5, mr + 1000]], dtype=np.int32)   # last one clamps to mr
+    ins = [device_slice(tr * size, r).view(tr, size) for r in range(n)]
+    tgs = [torch.full((tr, size), -7, dtype=torch.int32, device="cuda") for _ in range(n)]
+    sc = [torch.from_numpy(counts[s].copy()).cuda() for s in range(n)]
+    rc = [torch.zeros(n, dtype=torch.int32, device="cuda") for _ in range(n)]
+    P.ptoc_all_to_all_v(ins, tgs, sc, rc, tr, size, P.I32)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(8)
+    for d in range(n):
+        assert rc[d].cpu().tolist() == [int(min(max(counts[s][d], 0), mr)) for s in range(n)]
+        for s in range(n):
+            c = int(min(max(counts[s][d], 0), mr))
+            rows = {0, c - 1, c, mr - 1} | set(rng.integers(0, mr, size=40).tolist())
+            for i in sorted(x for x in rows if 0 <= x < mr):
+                got = tgs[d][s * mr + i]
+                if i < c:
+                    assert torch.equal(got, ins[s][d * mr + i]), (d, s, i)
+                else:
+                    assert bool((got == -7).all()), (d, s, i)
+    del ins, tgs
+    torch.cuda.empty_cache()
