@@ -233,8 +233,23 @@ def _rows_cols_ld(t):
     return t.shape[0], t.shape[1], t.stride(0)
 
 
+def _same_layout(tensors, what, contiguous=False):
+    """Every tensor 2-D with the first one's shape, row pitch, dtype and device
+    (and packed rows when `contiguous`): the C calls take one description."""
+    t0 = tensors[0]
+    rows, cols, ld = _rows_cols_ld(t0)
+    if contiguous and ld != cols:
+        raise ValueError("%s: rows must be packed (stride(0) == shape[1])" % what)
+    for t in tensors[1:]:
+        if t.dim() != 2 or tuple(t.shape) != tuple(t0.shape) or t.stride() != t0.stride() \
+                or t.dtype != t0.dtype or t.device != t0.device:
+            raise ValueError("%s: every tensor needs the same shape, strides, dtype and device" % what)
+    return rows, cols, ld
+
+
 def treduce(tensors, dst, op="sum", valid_rows=None, valid_cols=None, root=0, stream=None):
     """dst = reduction of 2-D tensors over their valid box (default: all)."""
+    _same_layout(list(tensors) + [dst], "treduce")
     rows, cols, ld = _rows_cols_ld(dst)
     vr = rows if valid_rows is None else valid_rows
     vc = cols if valid_cols is None else valid_cols
@@ -243,42 +258,42 @@ def treduce(tensors, dst, op="sum", valid_rows=None, valid_cols=None, root=0, st
 
 
 def reduce_scatter(windows, op="sum", stream=None):
-    rows, cols, ld = _rows_cols_ld(windows[0])
+    rows, cols, ld = _same_layout(windows, "reduce_scatter")
     return ptoc_reduce_scatter(windows, rows, cols, ld, OPS[op] if isinstance(op, str) else op,
                                dtype_code(windows[0]), stream=stream)
 
 
 def allgather(windows, stream=None):
-    rows, cols, ld = _rows_cols_ld(windows[0])
+    rows, cols, ld = _same_layout(windows, "allgather")
     return ptoc_allgather(windows, rows, cols, ld, dtype_code(windows[0]), stream=stream)
 
 
 def all_to_all_v(inputs, targets, send_counts, recv_counts, stream=None, noalloc=False):
     """noalloc=True: ptoc_all_to_all_v_noalloc (no allocation; one call in
     flight at a time)."""
-    tr, size = targets[0].shape
+    tr, size, _ = _same_layout(list(inputs) + list(targets), "all_to_all_v", contiguous=True)
     f = ptoc_all_to_all_v_noalloc if noalloc else ptoc_all_to_all_v
     return f(inputs, targets, send_counts, recv_counts, tr, size, dtype_code(targets[0]), stream=stream)
 
 
 def allreduce(windows, op="sum", stream=None):
-    rows, cols, ld = _rows_cols_ld(windows[0])
+    rows, cols, ld = _same_layout(windows, "allreduce")
     return ptoc_allreduce(windows, rows, cols, ld, OPS[op] if isinstance(op, str) else op,
                           dtype_code(windows[0]), stream=stream)
 
 
 def broadcast(windows, root=0, stream=None):
-    rows, cols, ld = _rows_cols_ld(windows[0])
+    rows, cols, ld = _same_layout(windows, "broadcast")
     return ptoc_broadcast(windows, rows, cols, ld, dtype_code(windows[0]), stream=stream, root=root)
 
 
 def all_to_all(inputs, targets, stream=None):
-    tr, size = targets[0].shape
+    tr, size, _ = _same_layout(list(inputs) + list(targets), "all_to_all", contiguous=True)
     return ptoc_all_to_all(inputs, targets, tr, size, dtype_code(targets[0]), stream=stream)
 
 
 def all_to_all_v_combine(windows, outputs, recv_counts, atomic="none", stream=None):
-    tr, size = outputs[0].shape
+    tr, size, _ = _same_layout(list(windows) + list(outputs), "all_to_all_v_combine", contiguous=True)
     a = {"none": ATOMIC_NONE, "add": ATOMIC_ADD}[atomic] if isinstance(atomic, str) else atomic
     return ptoc_all_to_all_v_combine(windows, outputs, recv_counts, tr, size, a,
                                      dtype_code(outputs[0]), stream=stream)
