@@ -204,9 +204,10 @@ cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, i
 {
     p.ld = ld;
     p.rows = rows;
-    // 9 to 16 ranks: 8-byte vectors, so all their loads fit in flight at once
-    // in the registers of one group of 16-byte loads
-    if (p.nranks > kGroup && p.nranks <= 2 * kGroup && vb > 8) vb = 8;
+    // 13 to 16 ranks: 8-byte vectors, so all their loads fit in flight at
+    // once in the registers of one group of 16-byte loads (9 to 12 ranks keep
+    // 16-byte vectors in a 12-slot form)
+    if (p.nranks > 12 && p.nranks <= 2 * kGroup && vb > 8) vb = 8;
     const Box b = make_box(rows, cols, ld, eb, vb, kBlock);
     p.vpr = b.vpr;
     p.tail = b.tail;

@@ -454,14 +454,17 @@ cudaError_t launch_kernel(K kernel, dim3 grid, unsigned block, size_t smem, cuda
 
 // How a thread covers the ranks (chosen on the host from the rank count):
 //   kOneGroup  up to kGroup ranks: all loads issued back to back, then folded.
-//   kWide      up to 2 * kGroup ranks on vectors of at most 8 bytes: the same,
-//              with all 2 * kGroup loads in flight (the host narrows 16-byte
-//              vectors to 8 so the registers stay those of one group).
+//   kWide12    9 to 12 ranks on 16-byte vectors: the same with 12 slots
+//              (80 registers: three blocks per SM, up to 192 bytes of loads in
+//              flight per thread).
+//   kWide      up to 2 * kGroup ranks on vectors of at most 8 bytes: all
+//              2 * kGroup loads in flight (the host narrows 16-byte vectors to
+//              8 for 13 to 16 ranks, so the registers stay those of one group).
 //   kGroups    more ranks: groups of kGroup, each issued and then folded.
-enum RankForm : int { kOneGroup = 0, kWide = 1, kGroups = 2 };
+enum RankForm : int { kOneGroup = 0, kWide = 1, kGroups = 2, kWide12 = 3 };
 
 template <int FORM>
-constexpr int kSlots = FORM == kWide ? 2 * kGroup : kGroup;
+constexpr int kSlots = FORM == kWide ? 2 * kGroup : FORM == kWide12 ? 12 : kGroup;
 
 // One tile: kBlock vectors of VB bytes of one row segment, one per thread,
 // folded in rank order 0, 1, 2, ... whatever the form.
@@ -559,8 +562,12 @@ cudaError_t launch_reduce_vb(const ReduceParams& p, dim3 grid, cudaStream_t s)
     if constexpr (VB >= 4) {
         if (p.nranks > 2 * kGroup) return launch_kernel(reduce_kernel<T, OP, VB, kGroups>, grid, kBlock, 0, s, p);
         if (p.nranks > kGroup) {
-            if constexpr (VB == 16) return cudaErrorInvalidValue;
-            else return launch_kernel(reduce_kernel<T, OP, VB, kWide>, grid, kBlock, 0, s, p);
+            if constexpr (VB == 16) {
+                if (p.nranks <= 12) return launch_kernel(reduce_kernel<T, OP, VB, kWide12>, grid, kBlock, 0, s, p);
+                return cudaErrorInvalidValue;
+            } else {
+                return launch_kernel(reduce_kernel<T, OP, VB, kWide>, grid, kBlock, 0, s, p);
+            }
         }
     }
     return launch_kernel(reduce_kernel<T, OP, VB, kOneGroup>, grid, kBlock, 0, s, p);
