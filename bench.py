@@ -235,7 +235,7 @@ class RsAgBench(Workload):
 
     def __init__(self):
         import synth
-        self.cfg = synth.CONFIG4
+        self.cfg = synth.WINDOWS_F16_N8_8192X4096
         self.name = "reduce_scatter_allgather_n8_f16_8192x4096"
         self.per_launch_timing = True
         self.storage = "f16"
@@ -339,7 +339,7 @@ class A2avBench(Workload):
 
     def __init__(self, count_div=1):
         import synth
-        self.cfg = synth.CONFIG5
+        self.cfg = synth.DISPATCH_BF16_N16_7168
         self.count_div = count_div
         self.name = ("all_to_all_v_n16_bf16_7168_maxrecv1536" if count_div == 1 else
                      "all_to_all_v_sparse_n16_bf16_7168_maxrecv1536_counts_div%d" % count_div)
@@ -462,7 +462,7 @@ class WindowOpBench(Workload):
     def __init__(self, op):
         import synth
         self.op = op
-        self.cfg = synth.CONFIG4
+        self.cfg = synth.WINDOWS_F16_N8_8192X4096
         self.name = "%s_n8_f16_8192x4096" % op
         self.storage = "f16"
         self.kernel = ("reduce_kernel<f16> (all-windows mode)" if op == "allreduce"
@@ -759,13 +759,13 @@ def make_workload(name, rows_div=1):
     import synth
     wl = None
     if name in ("treduce", "treduce_bf16"):
-        wl = TreduceBench(synth.config2(), "bf16")
+        wl = TreduceBench(synth.treduce_bf16_n8_4096_valid4000(), "bf16")
     elif name == "treduce_small":
-        wl = TreduceBench(synth.config1(), "f32")
+        wl = TreduceBench(synth.treduce_f32_n4_256(), "f32")
     elif name == "treduce_f32":
-        wl = TreduceBench(synth.config3(), "f32")
+        wl = TreduceBench(synth.treduce_f32_n8_16384x8192(), "f32")
     elif name == "treduce_i32":
-        wl = TreduceBench(synth.config3_int(), "i32")
+        wl = TreduceBench(synth.treduce_i32_n8_16384x8192(), "i32")
     elif name == "rs_ag":
         wl = RsAgBench()
     elif name == "a2av":

@@ -173,41 +173,41 @@ class TreduceWorkload:
         return values_at(self.dist, self.dtype, BASE_SEED + r, k)
 
 
-# The five configurations (shapes, distributions and sentinels).
-def config1():
+# The benchmark workloads: shapes, distributions and sentinels.
+def treduce_f32_n4_256():
     return TreduceWorkload("treduce_sum_n4_f32_256x256", 4, DT_F32, 256, 256, 256, 256, 256,
                            ("uniform", -1.0, 1.0), ["sum"])
 
 
-def config2():
+def treduce_bf16_n8_4096_valid4000():
     return TreduceWorkload("treduce_n8_bf16_4096x4096_valid4000", 8, DT_BF16, 4096, 4096, 4096,
                            4000, 4000, ("normal", 0, 1), ["sum", "max", "min"],
                            src_pad=0x7FD5, dst_pad=0xFFD5)
 
 
-def config3():
+def treduce_f32_n8_16384x8192():
     return TreduceWorkload("treduce_sum_n8_f32_16384x8192", 8, DT_F32, 16384, 8192, 8192,
                            16384, 8192, ("uniform", -1e3, 1e3), ["sum"])
 
 
-def config3_int():
+def treduce_i32_n8_16384x8192():
     return TreduceWorkload("treduce_max_n8_i32_16384x8192", 8, DT_I32, 16384, 8192, 8192,
                            16384, 8192, ("uniform", -2**30, 2**30), ["max"])
 
 
-CONFIG4 = dict(nranks=8, rows=8192, cols=4096, ld=4096, dtype=DT_F16, dist=("normal", 0, 1))
+WINDOWS_F16_N8_8192X4096 = dict(nranks=8, rows=8192, cols=4096, ld=4096, dtype=DT_F16, dist=("normal", 0, 1))
 
 
-def window(r, cfg=CONFIG4):
+def window(r, cfg=WINDOWS_F16_N8_8192X4096):
     return rank_slice(cfg["dist"], cfg["dtype"], r, cfg["rows"], cfg["ld"], cfg["rows"], cfg["cols"])
 
 
 # all_to_all_v: N=16 ranks, bf16 rows of 7168, target_rows 24576 (MAX_RECV 1536).
-CONFIG5 = dict(nranks=16, size=7168, target_rows=24576, count_hi=2047, sentinel=0xFFFF)
+DISPATCH_BF16_N16_7168 = dict(nranks=16, size=7168, target_rows=24576, count_hi=2047, sentinel=0xFFFF)
 COUNT_STREAM_START = 1 << 40   # counts use the sender's stream, far from its row data
 
 
-def a2av_send_counts(s, nranks, hi=CONFIG5["count_hi"], lo=0):
+def a2av_send_counts(s, nranks, hi=DISPATCH_BF16_N16_7168["count_hi"], lo=0):
     """send_counts of sender s: nranks ints uniform in [lo, hi]."""
     return fill(UNIF_I32, BASE_SEED + s, nranks, start=COUNT_STREAM_START, lo_i=lo, hi_i=hi)
 

@@ -141,11 +141,11 @@ def test_all_to_all_v_small(case):
 
 # ---- full-size workloads -----------------------------------------------------------
 
-def test_workload_4_reduce_scatter_allgather_full():
+def test_reduce_scatter_allgather_f16_n8_8192x4096_full():
     """8 windows fp16 [8192, 4096], N(0, 1): reduce_scatter (Sum, 1024-row
     chunks) then allgather, every element of every window against the oracle;
     and the gathered windows equal a TREDUCE of saved copies of the inputs."""
-    cfg = synth.CONFIG4
+    cfg = synth.WINDOWS_F16_N8_8192X4096
     n, rows, cols, ld = cfg["nranks"], cfg["rows"], cfg["cols"], cfg["ld"]
     host = [synth.window(r) for r in range(n)]
     dev = [to_dev(h) for h in host]
@@ -165,12 +165,12 @@ def test_workload_4_reduce_scatter_allgather_full():
         assert bool(torch.equal(dev[r], full))
 
 
-def test_workload_5_all_to_all_v_full():
+def test_all_to_all_v_bf16_n16_7168_full():
     """16 ranks, bf16 rows of 7168, target_rows 24576 (MAX_RECV 1536),
     send_counts uniform in [0, 2047] (about a quarter clamp), tagged input rows,
     targets prefilled with 0xFFFF: every target window and every count against
     the oracle."""
-    cfg = synth.CONFIG5
+    cfg = synth.DISPATCH_BF16_N16_7168
     n, tr, size = cfg["nranks"], cfg["target_rows"], cfg["size"]
     mr = tr // n
     inputs = [synth.a2av_input(s, n, tr, size) for s in range(n)]

@@ -207,9 +207,9 @@ def _upload(w):
     return host, [to_dev(h) for h in host]
 
 
-def test_workload_1_full():
+def test_treduce_f32_n4_256_full():
     """4 ranks, f32 256 x 256, U[-1, 1], Sum: every element against the oracle."""
-    w = synth.config1()
+    w = synth.treduce_f32_n4_256()
     host, dev = _upload(w)
     dst = torch.empty(w.rows, w.ld, dtype=torch.float32, device="cuda")
     P.ptoc_treduce(dev, dst, w.rows, w.cols, w.valid_rows, w.valid_cols, w.ld, P.SUM, P.F32)
@@ -219,11 +219,11 @@ def test_workload_1_full():
     assert np.array_equal(bits(got), bits(want)), first_diff(got, want)
 
 
-def test_workload_2_full():
+def test_treduce_bf16_n8_4096_valid4000_full():
     """8 ranks, bf16 [4096, 4096], valid 4000 x 4000 inside NaN-sentinel
     padding, N(0, 1); Sum, Max, Min: every element of dst (valid box and the
     untouched 0xFFD5 padding) against the oracle."""
-    w = synth.config2()
+    w = synth.treduce_bf16_n8_4096_valid4000()
     host, dev = _upload(w)
     for op in w.ops:
         want = np.full((w.rows, w.ld), w.dst_pad, dtype=np.uint16)
@@ -242,11 +242,11 @@ def _sample_points(rng, rows, cols, k):
     return ii, jj
 
 
-def test_workload_3_f32_sum_full_size():
+def test_treduce_f32_sum_n8_16384x8192_full():
     """8 ranks, f32 [16384, 8192] (4 GiB of inputs), U[-1e3, 1e3], Sum.
     Sampled elements against the oracle bit for bit, and every element within
     the recursive-summation bound of a binary64 sum."""
-    w = synth.config3()
+    w = synth.treduce_f32_n8_16384x8192()
     host, dev = _upload(w)
     dst = torch.empty(w.rows, w.ld, dtype=torch.float32, device="cuda")
     P.ptoc_treduce(dev, dst, w.rows, w.cols, w.valid_rows, w.valid_cols, w.ld, P.SUM, P.F32)
@@ -267,11 +267,11 @@ def test_workload_3_f32_sum_full_size():
     assert bool(torch.all(err <= (w.nranks - 1) * 2.0 ** -24 * mag * (1 + 1e-6) + 1e-300))
 
 
-def test_workload_3_i32_max_full_size():
+def test_treduce_i32_max_n8_16384x8192_full():
     """8 ranks, int32 [16384, 8192], U[-2^30, 2^30], Max: every element equal
     to the element-wise maximum (torch.maximum chain), sampled elements
     against the oracle."""
-    w = synth.config3_int()
+    w = synth.treduce_i32_n8_16384x8192()
     host, dev = _upload(w)
     dst = torch.empty(w.rows, w.ld, dtype=torch.int32, device="cuda")
     P.ptoc_treduce(dev, dst, w.rows, w.cols, w.valid_rows, w.valid_cols, w.ld, P.MAX, P.I32)

@@ -165,7 +165,7 @@ def test_dispatch_then_combine(atomic, dtype, case):
 def test_allreduce_full_size_f16():
     """8 windows fp16 [8192, 4096], N(0, 1), Sum: every element of every window
     against the oracle, and equal to reduce_scatter + allgather on the GPU."""
-    cfg = synth.CONFIG4
+    cfg = synth.WINDOWS_F16_N8_8192X4096
     n, rows, cols, ld = cfg["nranks"], cfg["rows"], cfg["cols"], cfg["ld"]
     host = [synth.window(r) for r in range(n)]
     dev = [to_dev(h) for h in host]
@@ -181,7 +181,7 @@ def test_allreduce_full_size_f16():
 
 
 def test_broadcast_full_size_f16():
-    cfg = synth.CONFIG4
+    cfg = synth.WINDOWS_F16_N8_8192X4096
     n, rows, cols, ld = cfg["nranks"], cfg["rows"], cfg["cols"], cfg["ld"]
     dev = [to_dev(synth.window(r)) for r in range(n)]
     root_copy = dev[3].clone()
@@ -193,7 +193,7 @@ def test_broadcast_full_size_f16():
 def test_all_to_all_full_size():
     """16 ranks, bf16 rows of 7168, target_rows 24576 (chunks of 1536 rows),
     tagged rows: every target against the oracle."""
-    cfg = synth.CONFIG5
+    cfg = synth.DISPATCH_BF16_N16_7168
     n, tr, size = cfg["nranks"], cfg["target_rows"], cfg["size"]
     inputs = [synth.a2av_input(s, n, tr, size) for s in range(n)]
     d_in = [to_dev(x) for x in inputs]
@@ -210,7 +210,7 @@ def test_dispatch_combine_full_size_bf16():
     """The MoE shape: 16 ranks, bf16 rows of 7168, MAX_RECV 1536, counts
     uniform in [0, 2047]. Dispatch, then combine with kAdd into outputs that
     hold other values; every output element against the oracle."""
-    cfg = synth.CONFIG5
+    cfg = synth.DISPATCH_BF16_N16_7168
     n, tr, size = cfg["nranks"], cfg["target_rows"], cfg["size"]
     inputs = [synth.values(("normal", 0, 1), synth.DT_BF16, 1234 + s, tr * size).reshape(tr, size)
               for s in range(n)]
