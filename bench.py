@@ -14,7 +14,7 @@ no dirty flush lines for the timed kernels to write back). Other workloads
 (the parity configurations) can be timed with --workload for the per-kernel
 evidence.
 
---impl reference times the CPU oracle on this machine's host cores (the only
+--impl reference times the CPU oracle on the host's CPU cores (the only
 other implementation there is), on a bounded sample of the same workload per
 step. Multi-GPU (torchrun): every rank runs an independent replica (the path
 has no cross-GPU exchange); value is the total over ranks / max time.

@@ -1,7 +1,7 @@
 """The C ABI without a GPU: the library loads, exports every function
 include/ptoc.h declares, and rejects bad arguments with the documented status
 before any CUDA call. Every case here breaks at least one rule (or is empty),
-so no case can reach a kernel launch, on this machine or on a GPU machine.
+so no case can reach a kernel launch, with or without a GPU.
 Device addresses below are fake and never dereferenced."""
 import ctypes
 import os
