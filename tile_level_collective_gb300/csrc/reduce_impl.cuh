@@ -15,13 +15,13 @@
 // segment of kBlock vectors of VB bytes, one per thread); each thread issues
 // the loads of a group of up to kGroup ranks back to back (kGroup independent
 // 16-byte loads in flight per thread) and only then folds them into its
-// accumulator in rank order (9 to 16 ranks: 8-byte vectors, all 16 loads in
-// flight; more ranks: one group after another). The grid has one block per tile, so as blocks
-// retire the hardware block scheduler hands the next tiles, in order, to
-// whichever SM has room. Accumulation is binary32
-// for every floating type (one RNE narrowing at the store); 16-bit Max / Min
-// compare packed pairs and select the raw encodings, so their result is the
-// selected input bit for bit.
+// accumulator in rank order (9 to 12 ranks: 12 slots of 16 bytes; 13 to 16:
+// 8-byte vectors, all 16 loads in flight; more ranks: one group after
+// another). The grid has one block per tile, so as blocks retire the hardware
+// block scheduler hands the next tiles, in order, to whichever SM has room.
+// Accumulation is binary32 for every floating type (one RNE narrowing at the
+// store); 16-bit Max / Min compare packed pairs and select the raw encodings,
+// so their result is the selected input bit for bit.
 #pragma once
 
 #include <cuda_bf16.h>
