@@ -1,6 +1,6 @@
 // Internal declarations shared by the library's translation units: kernel
-// parameter blocks (passed by value, so a call needs no device allocation) and
-// the per-dtype launchers the C-ABI layer dispatches to.
+// parameter blocks (passed by value, so they need no device memory) and the
+// per-dtype launchers the C-ABI layer dispatches to.
 #pragma once
 
 #include <cstdint>
@@ -21,7 +21,7 @@ enum Op : int { kSum = 0, kMax = 1, kMin = 2, kProd = 3 };
 // (reduce_scatter), or every window (allreduce).
 enum DstMode : int { kDstOne = 0, kDstOwner = 1, kDstAll = 2 };
 
-// TREDUCE and reduce_scatter. The box is `rows` rows of `vpr` full vectors of
+// TREDUCE, reduce_scatter and allreduce. The box is `rows` rows of `vpr` full vectors of
 // VB bytes plus `tail` trailing elements; one tile is one row segment of
 // kBlock vectors; the row tails are reduced by tail_blocks extra blocks.
 struct ReduceParams {
