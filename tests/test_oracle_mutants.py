@@ -30,6 +30,12 @@ MUTANTS = {
         "int shift = (e >= -14) ? 13 : (-1 - e);", "int shift = (e >= -14) ? 13 : (-e);"),
     "f16 widening exponent off by one": (
         "v = ldexpf((float)(1024 + m), e - 25);", "v = ldexpf((float)(1024 + m), e - 24);"),
+    "16-bit Sum rounds to the output type after every add": (
+        "if (op == ORC_SUM) acc = acc + widen(dtype, src[order[t]], k);",
+        "if (op == ORC_SUM) { uint32_t tmp = 0; acc = acc + widen(dtype, src[order[t]], k);"
+        " narrow_store(dtype, &tmp, 0, acc); acc = widen(dtype, &tmp, 0); }"),
+    "floating accumulator kept in double": (
+        "float acc = widen(dtype, src[order[0]], k);", "double acc = widen(dtype, src[order[0]], k);"),
     "Prod adds instead of multiplying": (
         "else acc = acc * widen(dtype, src[order[t]], k);", "else acc = acc + widen(dtype, src[order[t]], k);"),
     "treduce writes one column past the valid box": (
