@@ -1,6 +1,6 @@
 """Seeded random configurations of every data entry point against the oracle:
 rank counts from 1 to 20 (both reduction forms and the rank groups beyond
-them), ragged shapes, pitches wider than the rows, valid boxes from empty to
+them), ragged shapes, pitches wider than the rows, rows of several tiles, valid boxes from empty to
 full, every root, buffers placed off the 16-byte grid (so every vector width
 runs), Max / Min / Sum / Prod, and exchange counts that are negative, zero,
 within and beyond capacity. Every buffer carries guard bands; results must
@@ -49,14 +49,36 @@ def test_fuzz_treduce(seed):
                  seed=int(rng.integers(1 << 30)), specials=True)
 
 
+def wide_shape(rng):
+    """Rows wider than one tile (256 vectors), so that the pitched path
+    splits every row into several tiles plus a ragged last one."""
+    rows = int(rng.integers(1, 12))
+    cols = int(rng.integers(1000, 5000))
+    return rows, cols, cols + int(rng.integers(1, 9))
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_fuzz_treduce_wide_rows(seed):
+    rng = np.random.default_rng(1500 + seed)
+    for _ in range(40):
+        dtype = DTYPES[int(rng.integers(4))]
+        op = ["sum", "max", "min"][int(rng.integers(3))]
+        n = int(rng.integers(1, 21))
+        rows, cols, ld = wide_shape(rng)
+        vr, vc = int(rng.integers(1, rows + 1)), int(rng.integers(1, cols + 1))
+        run_case(dtype, op, n, rows, cols, ld, vr, vc, root=int(rng.integers(n)),
+                 offset=offset(rng, ELEM_BYTES[dtype]), inplace=bool(rng.random() < 0.2),
+                 seed=int(rng.integers(1 << 30)), specials=True)
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_fuzz_window_collectives(seed):
     """reduce_scatter then allgather, allreduce, and broadcast on random windows."""
     rng = np.random.default_rng(2000 + seed)
-    for _ in range(60):
+    for i in range(60):
         dtype = DTYPES[int(rng.integers(4))]
         n = int(rng.integers(1, 21))
-        rows, cols, ld = shape(rng)
+        rows, cols, ld = wide_shape(rng) if i % 6 == 5 else shape(rng)
         off = offset(rng, ELEM_BYTES[dtype])
         what = ["rs_ag", "allreduce", "broadcast"][int(rng.integers(3))]
         host = windows_host(dtype, n, rows, cols, ld, seed=int(rng.integers(1 << 30)))
@@ -96,6 +118,21 @@ def test_fuzz_all_to_all_v(seed):
         lo, hi = -int(rng.integers(0, 4)), mr + int(rng.integers(0, 6))
         run_a2av(n, tr, size, elem, lo, hi, seed=int(rng.integers(1 << 30)),
                  offset=offset(rng, np.dtype(elem).itemsize))
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_fuzz_all_to_all_v_wide_rows(seed):
+    """Rows of 4 to 36 KB: every pair's run spans several tiles, and the
+    tiles cross row boundaries."""
+    rng = np.random.default_rng(3500 + seed)
+    for _ in range(24):
+        n = int(rng.integers(1, 17))
+        tr = int(rng.integers(n, 6 * n + 1))
+        size = int(rng.integers(2000, 9000))
+        elem = [np.uint16, np.float32][int(rng.integers(2))]
+        mr = tr // n
+        run_a2av(n, tr, size, elem, -int(rng.integers(0, 3)), mr + int(rng.integers(0, 3)),
+                 seed=int(rng.integers(1 << 30)), offset=offset(rng, np.dtype(elem).itemsize))
 
 
 @pytest.mark.parametrize("seed", range(3))
