@@ -165,17 +165,20 @@ def test_reduce_scatter_allgather_f16_n8_8192x4096_full():
         assert bool(torch.equal(dev[r], full))
 
 
-def test_all_to_all_v_bf16_n16_7168_full():
+@pytest.mark.parametrize("count_div", [1, 64])
+def test_all_to_all_v_bf16_n16_7168_full(count_div):
     """16 ranks, bf16 rows of 7168, target_rows 24576 (MAX_RECV 1536),
     send_counts uniform in [0, 2047] (about a quarter clamp), tagged input rows,
     targets prefilled with 0xFFFF: every target window and every count against
-    the oracle."""
+    the oracle. With the counts divided by 64 it is the sparse exchange
+    (about 1 % of capacity) that the benchmark also times."""
     cfg = synth.DISPATCH_BF16_N16_7168
     n, tr, size = cfg["nranks"], cfg["target_rows"], cfg["size"]
     mr = tr // n
     inputs = [synth.a2av_input(s, n, tr, size) for s in range(n)]
-    sc = [synth.a2av_send_counts(s, n) for s in range(n)]
-    assert sum(int((c > mr).sum()) for c in sc) > 0          # the clamp is exercised
+    sc = [synth.a2av_send_counts(s, n) // count_div for s in range(n)]
+    if count_div == 1:
+        assert sum(int((c > mr).sum()) for c in sc) > 0      # the clamp is exercised
     d_in = [to_dev(x) for x in inputs]
     d_tg = [torch.full((tr, size), -1, dtype=torch.int16, device="cuda") for _ in range(n)]
     d_sc = [to_dev(c) for c in sc]
