@@ -135,6 +135,35 @@ def test_fuzz_all_to_all_v_wide_rows(seed):
                  seed=int(rng.integers(1 << 30)), offset=offset(rng, np.dtype(elem).itemsize))
 
 
+@pytest.mark.parametrize("seed", range(2))
+def test_fuzz_combine_wide_rows(seed):
+    """The combine (kNone and kAdd) on rows of 4 to 36 KB, several tiles per
+    pair run."""
+    rng = np.random.default_rng(4500 + seed)
+    for _ in range(16):
+        dtype = DTYPES[int(rng.integers(4))]
+        eb = ELEM_BYTES[dtype]
+        n = int(rng.integers(1, 17))
+        tr = int(rng.integers(n, 6 * n + 1))
+        size = int(rng.integers(2000, 9000))
+        off = offset(rng, eb)
+        mr = tr // n
+        ins = [values(rng, dtype, (tr, size)) for _ in range(n)]
+        outs = [values(rng, dtype, (tr, size)) for _ in range(n)]
+        rc = [rng.integers(-1, mr + 2, size=n).astype(np.int32) for _ in range(n)]
+        atomic = [P.ATOMIC_NONE, P.ATOMIC_ADD][int(rng.integers(2))]
+        d_in = [DevBuf(x, off) for x in ins]
+        d_out = [DevBuf(o, off) for o in outs]
+        d_rc = [DevBuf(c) for c in rc]
+        P.ptoc_all_to_all_v_combine([d.ptr for d in d_in], [d.ptr for d in d_out], [d.ptr for d in d_rc],
+                                    tr, size, atomic, PCODE[dtype])
+        torch.cuda.synchronize()
+        assert oracle.all_to_all_v_combine(ins, outs, rc, tr, size, atomic, ORC_DT[dtype]) == 0
+        for s in range(n):
+            assert nan_equal(d_out[s].host(), outs[s], dtype), "combine %s atomic %d output %d" % (dtype, atomic, s)
+            assert d_out[s].guards_intact() and d_rc[s].guards_intact()
+
+
 @pytest.mark.parametrize("seed", range(3))
 def test_fuzz_all_to_all_and_combine(seed):
     """The symmetric all_to_all and the combine (kNone and kAdd) on random
