@@ -13,6 +13,8 @@ Entry points carry the C names:
     ptoc_allgather(windows, rows, cols, ld, dtype, stream=None)
     ptoc_all_to_all_v(inputs, targets, send_counts, recv_counts, target_rows,
                       size, dtype, stream=None)
+    ptoc_all_to_all_v_noalloc(inputs, targets, send_counts, recv_counts,
+                              target_rows, size, dtype, stream=None)
     ptoc_allreduce(windows, rows, cols, ld, op, dtype, stream=None)
     ptoc_broadcast(windows, rows, cols, ld, dtype, stream=None, root=0)
     ptoc_all_to_all(inputs, targets, target_rows, size, dtype, stream=None)
@@ -25,8 +27,11 @@ Entry points carry the C names:
 Buffers are torch tensors or raw device addresses (ints). ``stream=None``
 means torch's current stream. A non-OK status raises :class:`PtocError`
 (nothing was launched); pass ``check=False`` to get the status instead.
-``treduce`` / ``reduce_scatter`` / ``allgather`` / ``all_to_all_v`` are
-shape-inferring conveniences over the same calls.
+``treduce``, ``reduce_scatter``, ``allgather``, ``allreduce``, ``broadcast``,
+``all_to_all_v`` (``noalloc=True`` selects the no-allocation call),
+``all_to_all`` and ``all_to_all_v_combine`` are shape-inferring conveniences
+over the same calls; they refuse (ValueError) tensors whose layouts the C calls
+cannot describe.
 
 The package refuses to import when libptoc.so has not been built: there is no
 fallback path.
