@@ -948,6 +948,18 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+# A replica that dies or never reaches the timing exchange makes the others
+# fail with an error after this long instead of waiting for the backend's
+# default (ten minutes for NCCL).
+PG_TIMEOUT_S = 300
+
+
+def init_replicas(backend, timeout_s=PG_TIMEOUT_S, **kw):
+    import datetime
+    import torch.distributed as dist
+    dist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s), **kw)
+
+
 def aggregate(ms_local, bytes_per_step, world, device):
     """Whole-job figures of a replica run: the step time is the max over ranks
     and `value` counts the bytes every rank processed (weak scaling)."""
@@ -987,8 +999,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+        init_replicas("nccl")
 
     def barrier():
         if world > 1:

@@ -1,5 +1,6 @@
 """Host-side logic of the multi-GPU benchmark, on CPU: world-size-2 gloo ranks
-run bench.aggregate (max step time over ranks, whole-job value), the argument
+run bench.aggregate (max step time over ranks, whole-job value) and fail with an
+error, not a hang, when one rank leaves before the exchange; the argument
 parser keeps the driver's defaults, and the reference arm's JSON line has the
 keys the contract asks for."""
 import json
@@ -8,6 +9,7 @@ import socket
 import subprocess
 import sys
 
+import pytest
 import torch.multiprocessing as mp
 
 from conftest import ROOT
@@ -46,6 +48,41 @@ def test_aggregate_max_over_two_gloo_ranks():
         ms, value = got[rank]
         assert ms == 5.0                              # the max over ranks
         assert abs(value - 2 * 1e9 / 5e-3 / 1e9) < 1e-6  # both ranks' bytes / max time
+
+
+def _rank_leaves_early(rank, world, port, mode, results):
+    import time
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    bench.init_replicas("gloo", timeout_s=3, rank=rank, world_size=world)
+    if rank == 1:
+        if mode == "stalls":             # alive, but never reaches the exchange
+            time.sleep(8)
+        return                           # leaves before the timing exchange
+    t0 = time.time()
+    try:
+        bench.aggregate(2.0, 1_000_000_000, world, torch.device("cpu"))
+        results[rank] = ("no error", time.time() - t0)
+    except Exception as e:               # the backend reports the missing peer
+        results[rank] = (type(e).__name__, time.time() - t0)
+
+
+@pytest.mark.parametrize("mode", ["exits", "stalls"])
+def test_a_replica_that_leaves_makes_the_others_fail_not_hang(mode):
+    """A rank that exits, or stalls, before the max-over-ranks exchange: the
+    remaining rank's exchange raises (a closed connection at once, or the
+    process group's 3 s timeout) instead of waiting."""
+    world, port = 2, _free_port()
+    with mp.Manager() as m:
+        results = m.dict()
+        mp.spawn(_rank_leaves_early, args=(world, port, mode, results), nprocs=world, join=True)
+        got = dict(results)
+    what, seconds = got[0]
+    assert what != "no error"
+    assert seconds < 10
 
 
 def test_defaults_and_reference_line():
