@@ -295,6 +295,31 @@ ptoc_status ptoc_credit_barrier(const ptoc_group* signals, const int32_t* local_
                                 cudaStream_t stream);
 
 /*
+ * ptoc_credit_barrier_host - the same credit barrier ([DO] "Barrier-signal
+ * protocol") for ranks that are host threads or host processes. The calling
+ * thread runs rank `rank`'s part of one call; every rank that takes part
+ * calls it once, with the same windows and `generations`.
+ *   signals->tensors[p] : HOST pointer to rank p's window of N int32 cells
+ *                         (memory every participant addresses: the memory
+ *                         of one process shared by its threads, or a mapping
+ *                         shared between processes). Cells are updated with
+ *                         lock-free 32-bit atomics; all must be zero when a
+ *                         call starts and are zero again after a complete
+ *                         call. signals->root is ignored.
+ *   status              : host int32; 0 if the rank completed, or g if it
+ *                         gave up waiting in generation g.
+ * Same steps as ptoc_credit_barrier (release adds, acquire waits for >= g,
+ * the epilogue subtracts `generations`). A rank that never calls never
+ * arrives: the others give up after timeout_ns (0 < timeout_ns <= 60 s, on
+ * the steady clock) and leave their credits, so zero the windows before the
+ * next call. Blocks the calling thread; makes no CUDA call and needs no GPU.
+ * Errors: invalid arguments (rank outside [0, N), null or misaligned
+ * pointers, sizes), overlapping windows or status (PTOC_ERR_ALIAS).
+ */
+ptoc_status ptoc_credit_barrier_host(const ptoc_group* signals, int32_t rank, int32_t generations,
+                                     int64_t timeout_ns, int32_t* status);
+
+/*
  * ptoc_signal_reset - zero every cell of every signal window on `stream`
  * (the host-side reset the page prescribes after an aborted call).
  */

@@ -25,7 +25,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert declared_functions() == ["ptoc_all_to_all", "ptoc_all_to_all_v", "ptoc_all_to_all_v_combine",
                                     "ptoc_all_to_all_v_noalloc", "ptoc_allgather", "ptoc_allreduce", "ptoc_broadcast",
-                                    "ptoc_credit_barrier", "ptoc_reduce_scatter", "ptoc_signal_reset",
+                                    "ptoc_credit_barrier", "ptoc_credit_barrier_host", "ptoc_reduce_scatter",
+                                    "ptoc_signal_reset",
                                     "ptoc_status_string", "ptoc_treduce"]
 
 

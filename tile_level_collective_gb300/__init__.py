@@ -22,6 +22,7 @@ Entry points carry the C names:
                               atomic, dtype, stream=None)
     ptoc_credit_barrier(signals, local_ranks, generations, timeout_ns, status,
                         stream=None)
+    ptoc_credit_barrier_host(signals, rank, generations, timeout_ns, status)
     ptoc_signal_reset(signals, stream=None)
 
 Buffers are torch tensors or raw device addresses (ints). ``stream=None``
@@ -80,10 +81,11 @@ _lib.ptoc_all_to_all_v_combine.argtypes = [_G, _G, ctypes.POINTER(_vp), _i64, _i
                                            ctypes.c_int, _vp]
 _lib.ptoc_credit_barrier.argtypes = [_G, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                      _i64, _vp, _vp]
+_lib.ptoc_credit_barrier_host.argtypes = [_G, ctypes.c_int32, ctypes.c_int32, _i64, _vp]
 _lib.ptoc_signal_reset.argtypes = [_G, _vp]
 for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to_all_v", "ptoc_all_to_all_v_noalloc",
            "ptoc_allreduce", "ptoc_broadcast", "ptoc_all_to_all", "ptoc_all_to_all_v_combine",
-           "ptoc_credit_barrier", "ptoc_signal_reset"):
+           "ptoc_credit_barrier", "ptoc_credit_barrier_host", "ptoc_signal_reset"):
     getattr(_lib, _f).restype = ctypes.c_int
 _lib.ptoc_status_string.argtypes = [ctypes.c_int]
 _lib.ptoc_status_string.restype = ctypes.c_char_p
@@ -212,6 +214,17 @@ def ptoc_credit_barrier(signals, local_ranks, generations, timeout_ns, status, s
     st = _lib.ptoc_credit_barrier(ctypes.byref(g), ranks, len(local_ranks), int(generations),
                                   int(timeout_ns), _addr(status), _stream(stream))
     return _done(st, "ptoc_credit_barrier", check)
+
+
+def ptoc_credit_barrier_host(signals, rank, generations, timeout_ns, status, check=True):
+    """Rank `rank`'s part of one host credit-barrier call, on the calling
+    thread. `signals` and `status` are HOST addresses (ints) or CPU tensors.
+    ctypes releases the GIL for the call, so ranks on Python threads run
+    concurrently."""
+    g, keep = _group(signals)
+    st = _lib.ptoc_credit_barrier_host(ctypes.byref(g), int(rank), int(generations), int(timeout_ns),
+                                       _addr(status))
+    return _done(st, "ptoc_credit_barrier_host", check)
 
 
 def ptoc_signal_reset(signals, stream=None, check=True):
