@@ -72,6 +72,8 @@ def load(path):
     L = ctypes.CDLL(path)
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     L.oracle_treduce.argtypes = [ctypes.POINTER(vp), i32, i32, vp, i64, i64, i64, i32, i32]
+    L.oracle_treduce_sum_native_acc.argtypes = [ctypes.POINTER(vp), i32, i32, vp, i64, i64, i64, i32]
+    L.oracle_treduce_sum_native_acc.restype = ctypes.c_int
     L.oracle_reduce_scatter.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32, i32]
     L.oracle_allgather.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, i32]
     L.oracle_all_to_all_v.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp),
@@ -113,6 +115,13 @@ def treduce(srcs, dst, valid_rows, valid_cols, ld, op, dtype, root=0):
     """dst[i*ld+j] = reduction over srcs in the page's rank order; see oracle.c."""
     return lib().oracle_treduce(_ptrs(srcs), len(srcs), root, dst.ctypes.data,
                                 valid_rows, valid_cols, ld, op, dtype)
+
+
+def treduce_sum_native_acc(srcs, dst, valid_rows, valid_cols, ld, dtype, root=0):
+    """TREDUCE Sum with every partial sum rounded to the destination type (the
+    accumulator tile in the destination type); see oracle.c."""
+    return lib().oracle_treduce_sum_native_acc(_ptrs(srcs), len(srcs), root, dst.ctypes.data,
+                                               valid_rows, valid_cols, ld, dtype)
 
 
 def reduce_scatter(windows, rows, cols, ld, op, dtype):

@@ -270,6 +270,43 @@ int oracle_treduce(const void* const* src, int nranks, int root, void* dst,
     return ORC_OK;
 }
 
+/*
+ * TREDUCE Sum under the other reading of the accumulator's precision: [TR]
+ * §3.1 declares the accumulator tile with the destination's element type, so
+ * every partial sum is rounded (RNE) to that type before the next rank is
+ * added. Ranks in the same order as oracle_treduce. For f32 the two readings
+ * coincide; Max and Min select an operand and are not affected. This is test
+ * infrastructure that measures what the binary32 accumulator changes; the
+ * library implements only the binary32 accumulator.
+ */
+int oracle_treduce_sum_native_acc(const void* const* src, int nranks, int root, void* dst,
+                                  int64_t valid_rows, int64_t valid_cols, int64_t ld, int dtype)
+{
+    if (nranks <= 0 || root < 0 || root >= nranks) return ORC_BAD_ARG;
+    if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16) return ORC_BAD_ARG;
+    if (valid_rows < 0 || valid_cols < 0 || (valid_cols > ld && valid_rows > 0)) return ORC_BAD_ARG;
+    if (valid_rows == 0 || valid_cols == 0) return ORC_OK;
+
+    int* order = (int*)malloc(sizeof(int) * (size_t)nranks);
+    if (!order) return ORC_BAD_ARG;
+    rank_order(nranks, root, order);
+    for (int64_t i = 0; i < valid_rows; ++i)
+        for (int64_t j = 0; j < valid_cols; ++j) {
+            const int64_t k = i * ld + j;
+            float acc = widen(dtype, src[order[0]], k);
+            for (int t = 1; t < nranks; ++t) {
+                const float sum = acc + widen(dtype, src[order[t]], k);
+                /* the accumulator tile holds the destination type */
+                if (dtype == ORC_BF16) acc = oracle_bf16_to_f32(oracle_f32_to_bf16(sum));
+                else if (dtype == ORC_F16) acc = oracle_f16_to_f32(oracle_f32_to_f16(sum));
+                else acc = sum;
+            }
+            narrow_store(dtype, dst, k, acc);
+        }
+    free(order);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* reduce_scatter and allgather over N windows                               */
 /* ------------------------------------------------------------------------ */
