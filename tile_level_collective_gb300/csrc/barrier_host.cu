@@ -17,6 +17,8 @@
 #include <cstdint>
 #include <thread>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ptoc.h"
 #include "ptoc_internal.h"
 
@@ -35,8 +37,8 @@ bool ranges_overlap(uintptr_t a, uintptr_t an, uintptr_t b, uintptr_t bn)
 
 }  // namespace
 
-extern "C" ptoc_status ptoc_credit_barrier_host(const ptoc_group* signals, int32_t rank, int32_t generations,
-                                                int64_t timeout_ns, int32_t* status)
+static ptoc_status credit_barrier_host(const ptoc_group* signals, int32_t rank, int32_t generations,
+                                       int64_t timeout_ns, int32_t* status)
 {
     if (!signals || !signals->tensors || !status) return PTOC_ERR_INVALID_ARG;
     const int n = signals->nranks;
@@ -82,4 +84,13 @@ extern "C" ptoc_status ptoc_credit_barrier_host(const ptoc_group* signals, int32
             if (s != me) credit_add(sig[me] + s, -generations);
     *status = st;
     return PTOC_OK;
+}
+
+extern "C" ptoc_status ptoc_credit_barrier_host(const ptoc_group* signals, int32_t rank, int32_t generations,
+                                                int64_t timeout_ns, int32_t* status)
+{
+    nvtxRangePushA("ptoc_credit_barrier_host");
+    const ptoc_status st = credit_barrier_host(signals, rank, generations, timeout_ns, status);
+    nvtxRangePop();
+    return st;
 }

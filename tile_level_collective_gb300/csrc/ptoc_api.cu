@@ -9,11 +9,22 @@
 #include <mutex>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "ptoc.h"
 #include "ptoc_internal.h"
 
 namespace ptoc {
+
+// A named NVTX range around the host side of every entry point (checks and
+// launches), so that timeline tools show the library's calls by name. With
+// no tool attached a range costs a few nanoseconds.
+struct TraceRange {
+    explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange&) = delete;
+    TraceRange& operator=(const TraceRange&) = delete;
+};
 
 bool programmatic_launch()
 {
@@ -353,6 +364,7 @@ extern "C" ptoc_status ptoc_treduce(const ptoc_group* group, void* dst, int64_t 
                                     int64_t valid_rows, int64_t valid_cols, int64_t ld,
                                     ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_treduce");
     ptoc_status st = check_group(group, true);
     if (st != PTOC_OK) return st;
     if (!dst) return PTOC_ERR_INVALID_ARG;
@@ -447,12 +459,14 @@ static ptoc_status window_reduction(const ptoc_group* windows, int64_t rows, int
 extern "C" ptoc_status ptoc_reduce_scatter(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
                                            ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_reduce_scatter");
     return window_reduction(windows, rows, cols, ld, op, dtype, stream, kDstOwner);
 }
 
 extern "C" ptoc_status ptoc_allreduce(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
                                       ptoc_reduce_op op, ptoc_dtype dtype, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_allreduce");
     return window_reduction(windows, rows, cols, ld, op, dtype, stream, kDstAll);
 }
 
@@ -490,6 +504,7 @@ static ptoc_status window_copy(const ptoc_group* windows, int64_t rows, int64_t 
 extern "C" ptoc_status ptoc_allgather(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
                                       ptoc_dtype dtype, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_allgather");
     int64_t fp = 0;
     ptoc_status st = check_windows(windows, rows, cols, ld, dtype, &fp);
     if (st != PTOC_OK) return st;
@@ -500,6 +515,7 @@ extern "C" ptoc_status ptoc_allgather(const ptoc_group* windows, int64_t rows, i
 extern "C" ptoc_status ptoc_broadcast(const ptoc_group* windows, int64_t rows, int64_t cols, int64_t ld,
                                       ptoc_dtype dtype, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_broadcast");
     ptoc_status st = check_group(windows, true);
     if (st != PTOC_OK) return st;
     int64_t fp = 0;
@@ -561,6 +577,7 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
                                          int64_t target_rows, int64_t size, ptoc_dtype dtype,
                                          cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_all_to_all_v");
     A2avParams p;
     int eb = 0;
     const ptoc_status st = a2av_setup(inputs, targets, send_counts, recv_counts, target_rows, size, dtype, p, eb);
@@ -597,6 +614,7 @@ extern "C" ptoc_status ptoc_all_to_all_v_noalloc(const ptoc_group* inputs, const
                                                  int64_t target_rows, int64_t size, ptoc_dtype dtype,
                                                  cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_all_to_all_v_noalloc");
     A2avParams p;
     int eb = 0;
     const ptoc_status st = a2av_setup(inputs, targets, send_counts, recv_counts, target_rows, size, dtype, p, eb);
@@ -616,6 +634,7 @@ extern "C" ptoc_status ptoc_all_to_all_v_noalloc(const ptoc_group* inputs, const
 extern "C" ptoc_status ptoc_all_to_all(const ptoc_group* inputs, const ptoc_group* targets,
                                        int64_t target_rows, int64_t size, ptoc_dtype dtype, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_all_to_all");
     ptoc_status st = check_pair_group(inputs, targets);
     if (st != PTOC_OK) return st;
     if (!valid_dtype(dtype)) return PTOC_ERR_INVALID_ARG;
@@ -655,6 +674,7 @@ extern "C" ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, cons
                                                  int64_t size, ptoc_atomic_type atomic, ptoc_dtype dtype,
                                                  cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_all_to_all_v_combine");
     ptoc_status st = check_pair_group(windows, outputs);
     if (st != PTOC_OK) return st;
     if (!recv_counts) return PTOC_ERR_INVALID_ARG;
@@ -698,6 +718,7 @@ extern "C" ptoc_status ptoc_credit_barrier(const ptoc_group* signals, const int3
                                            int32_t generations, int64_t timeout_ns, int32_t* status,
                                            cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_credit_barrier");
     ptoc_status st = check_group(signals, false);
     if (st != PTOC_OK) return st;
     const int n = signals->nranks;
@@ -737,6 +758,7 @@ extern "C" ptoc_status ptoc_credit_barrier(const ptoc_group* signals, const int3
 
 extern "C" ptoc_status ptoc_signal_reset(const ptoc_group* signals, cudaStream_t stream)
 {
+    const TraceRange trace("ptoc_signal_reset");
     ptoc_status st = check_group(signals, false);
     if (st != PTOC_OK) return st;
     const int n = signals->nranks;
