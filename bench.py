@@ -202,6 +202,26 @@ class TreduceBench(Workload):
         nb, dt, _ = self.oracle_sample(8)
         return 8.0 / max(dt, 1e-9)
 
+    def oracle_parity(self, rows):
+        """The resident run's results on the first `rows` rows against the
+        oracle on the same host inputs, bit for bit: every valid element, and
+        the padding of those rows still holding its sentinel."""
+        import numpy as np
+        import oracle
+        w = self.w
+        rows = max(1, min(rows, w.valid_rows))
+        code = {"f32": oracle.F32, "bf16": oracle.BF16, "f16": oracle.F16, "i32": oracle.I32}[self.storage]
+        ops = {"sum": oracle.SUM, "max": oracle.MAX, "min": oracle.MIN}
+        bad = []
+        for i, op in enumerate(w.ops):
+            want = self.dst_init[:rows].copy()
+            oracle.treduce([h[:rows] for h in self.host], want, rows, w.valid_cols, w.ld, ops[op], code)
+            got = np.ascontiguousarray(self.dsts[i][:rows].cpu().numpy()).view(want.dtype)
+            if not np.array_equal(got.view(np.uint8), want.view(np.uint8)):
+                bad.append(op)
+        return {"rows": "0..%d of %d" % (rows - 1, w.valid_rows), "ops": list(w.ops),
+                "result": "bit-exact" if not bad else "MISMATCH in " + ", ".join(bad)}
+
     def oracle_sample_threaded(self, rows, threads):
         """The same oracle call on `rows` rows, the rows split into `threads`
         contiguous slices run on as many host threads (ctypes releases the
@@ -979,6 +999,11 @@ def cpu_baseline(wl, budget_s):
         nb_tot, dt_tot, reps = nb_tot + nb, dt_tot + dt, reps + 1
     line = {"value": nb_tot / dt_tot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%s, %d repetition(s)" % (desc, reps), "seconds": round(dt_tot, 3)}
+    if hasattr(wl, "oracle_parity"):
+        # the same sample, untimed, against the resident run's results
+        line["parity"] = wl.oracle_parity(rows)
+        if line["parity"]["result"] != "bit-exact":
+            print("bench: results differ from the oracle: %s" % line["parity"], file=sys.stderr)
     if hasattr(wl, "oracle_sample_threaded"):
         # the same oracle over every host core, rows split into contiguous slices
         threads = os.cpu_count() or 1

@@ -85,6 +85,30 @@ def test_a_replica_that_leaves_makes_the_others_fail_not_hang(mode):
     assert seconds < 10
 
 
+def test_parity_leg_compares_the_resident_results():
+    """The CPU-baseline leg's parity check on host stand-ins for the resident
+    results: a correct result passes, one changed element fails, and a sample
+    that stops before the changed row passes."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    wl = bench.make_workload("treduce_small", 1)
+    wl.setup_host()
+    w = wl.w
+    wl.dst_init = np.zeros((w.rows, w.ld), dtype=wl.host[0].dtype)
+    good = wl.dst_init.copy()
+    assert oracle.treduce(wl.host, good, w.valid_rows, w.valid_cols, w.ld, oracle.SUM, oracle.F32) == 0
+    wl.dsts = [torch.from_numpy(good.copy())]
+    assert wl.oracle_parity(64)["result"] == "bit-exact"
+    bad = good.copy()
+    bad[3, 5] = np.nextafter(bad[3, 5], np.float32(10))
+    wl.dsts = [torch.from_numpy(bad)]
+    assert wl.oracle_parity(64)["result"] == "MISMATCH in sum"
+    assert wl.oracle_parity(3)["result"] == "bit-exact"
+
+
 def test_defaults_and_reference_line():
     sys.path.insert(0, ROOT)
     import bench
