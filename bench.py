@@ -339,13 +339,27 @@ class RsAgBench(Workload):
         c = self.cfg
         n = c["nranks"]
         rows = max(n, min(rows, c["rows"]))
-        wins = [np.ascontiguousarray(h[:rows]) for h in self.host]
+        wins = [h[:rows].copy() for h in self.host]          # the oracle works in place
         t0 = time.perf_counter()
         oracle.reduce_scatter(wins, rows, c["cols"], c["ld"], oracle.SUM, oracle.F16)
         oracle.allgather(wins, rows, c["cols"], c["ld"], oracle.F16)
         dt = time.perf_counter() - t0
         nb = (2 * n + 1) * 2 * rows * c["cols"]
         return nb, dt, "reduce_scatter+allgather over rows 0..%d of the 8 windows" % (rows - 1)
+
+    def oracle_parity(self, rows):
+        """After reduce_scatter and allgather every window holds, in each row,
+        the rank-ordered reduction of that row whatever the chunk bounds, so
+        the oracle's pass over the first rows gives the full-size values
+        there."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        rows = max(c["nranks"], min(rows, c["rows"]))
+        wins = [h[:rows].copy() for h in self.host]          # the oracle works in place
+        oracle.reduce_scatter(wins, rows, c["cols"], c["ld"], oracle.SUM, oracle.F16)
+        oracle.allgather(wins, rows, c["cols"], c["ld"], oracle.F16)
+        return _windows_parity(self.dev, wins, rows, c["rows"])
 
     def oracle_rows_per_second(self):
         nb, dt, _ = self.oracle_sample(64)
@@ -564,7 +578,7 @@ class WindowOpBench(Workload):
         import oracle
         c = self.cfg
         rows = max(1, min(rows, c["rows"]))
-        wins = [np.ascontiguousarray(h[:rows]) for h in self.host]
+        wins = [h[:rows].copy() for h in self.host]          # the oracle works in place
         t0 = time.perf_counter()
         if self.op == "allreduce":
             oracle.allreduce(wins, rows, c["cols"], c["ld"], oracle.SUM, oracle.F16)
@@ -574,6 +588,20 @@ class WindowOpBench(Workload):
         n = c["nranks"]
         nb = (2 * n if self.op == "allreduce" else n) * 2 * rows * c["cols"]
         return nb, dt, "%s over rows 0..%d of the 8 windows" % (self.op, rows - 1)
+
+    def oracle_parity(self, rows):
+        """Both operations act row by row, so the oracle's pass over the first
+        rows gives the full-size values there."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        rows = max(1, min(rows, c["rows"]))
+        wins = [h[:rows].copy() for h in self.host]          # the oracle works in place
+        if self.op == "allreduce":
+            oracle.allreduce(wins, rows, c["cols"], c["ld"], oracle.SUM, oracle.F16)
+        else:
+            oracle.broadcast(wins, 0, rows, c["cols"], c["ld"], oracle.F16)
+        return _windows_parity(self.dev, wins, rows, c["rows"])
 
     def oracle_rows_per_second(self):
         nb, dt, _ = self.oracle_sample(64)
@@ -724,7 +752,8 @@ class PairsBench(A2avBench):
             oracle.all_to_all(ins, tg, tr, size, 2)
             dt = time.perf_counter() - t0
             return 4 * size * n * n * mr, dt, "all_to_all with chunks of %d rows" % mr
-        outs = [np.ascontiguousarray(h.reshape(n, self.mr, size)[:, :mr].reshape(tr, size)) for h in self.out_host]
+        # a copy: the kAdd combine adds into its outputs in place
+        outs = [h.reshape(n, self.mr, size)[:, :mr].reshape(tr, size).copy() for h in self.out_host]
         rc = [np.clip(np.array(x), 0, self.mr).astype(np.int32) * mr // self.mr for x in self.sc]
         rc = [np.ascontiguousarray(np.array([rc[s][d] for s in range(n)], np.int32)) for d in range(n)]
         t0 = time.perf_counter()
@@ -855,6 +884,16 @@ def _check_same(pinned, refs, what):
     for i, (o, d) in enumerate(zip(pinned, refs)):
         if not bool((o == d.reshape(-1).view(torch_uint8()).cpu()).all()):
             raise RuntimeError("pipelined end-to-end %s %d differs from the resident result" % (what, i))
+
+
+def _windows_parity(dev_windows, want, rows, total_rows):
+    """The resident windows' first `rows` rows against the oracle's windows,
+    bit for bit."""
+    import numpy as np
+    bad = [r for r, (d, w) in enumerate(zip(dev_windows, want))
+           if not np.array_equal(np.ascontiguousarray(d[:rows].cpu().numpy()).view(np.uint8), w.view(np.uint8))]
+    return {"rows": "0..%d of %d" % (rows - 1, total_rows),
+            "result": "bit-exact" if not bad else "MISMATCH in windows " + ", ".join(map(str, bad))}
 
 
 def _pin(h):

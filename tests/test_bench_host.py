@@ -109,6 +109,51 @@ def test_parity_leg_compares_the_resident_results():
     assert wl.oracle_parity(3)["result"] == "bit-exact"
 
 
+@pytest.mark.parametrize("name", ["rs_ag", "allreduce", "broadcast"])
+def test_window_samples_leave_the_inputs_alone(name):
+    """The oracle works in place on windows: the CPU-baseline sample and the
+    parity check must run it on copies, so that repeated samples, and the
+    parity check after them, see the workload's own inputs (small windows
+    stand in for the 8 x 8192 x 4096 ones)."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    wl = bench.make_workload(name, 1)
+    wl.cfg = dict(wl.cfg, nranks=4, rows=12, cols=40, ld=40)
+    wl.setup_host()
+    before = [h.copy() for h in wl.host]
+    for _ in range(3):
+        wl.oracle_sample(12)
+    assert all(np.array_equal(a, b) for a, b in zip(before, wl.host))
+    want = [h.copy() for h in wl.host]
+    c = wl.cfg
+    if name == "rs_ag":
+        oracle.reduce_scatter(want, 12, 40, 40, oracle.SUM, oracle.F16)
+        oracle.allgather(want, 12, 40, 40, oracle.F16)
+    elif name == "allreduce":
+        oracle.allreduce(want, 12, 40, 40, oracle.SUM, oracle.F16)
+    else:
+        oracle.broadcast(want, 0, 12, 40, 40, oracle.F16)
+    wl.dev = [torch.from_numpy(w.view(np.int16).copy()) for w in want]      # stand-ins for the resident run
+    assert wl.oracle_parity(12)["result"] == "bit-exact"
+    assert wl.oracle_parity(5)["result"] == "bit-exact"
+    assert all(np.array_equal(a, b) for a, b in zip(before, wl.host))
+
+
+def test_windows_parity_helper():
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    want = [np.arange(40, dtype=np.uint16).reshape(5, 8) + r for r in range(3)]
+    dev = [torch.from_numpy(np.vstack([w.view(np.int16), np.zeros((2, 8), np.int16)])) for w in want]
+    assert bench._windows_parity(dev, want, 5, 7)["result"] == "bit-exact"
+    dev[2][4, 7] += 1
+    assert bench._windows_parity(dev, want, 5, 7)["result"] == "MISMATCH in windows 2"
+
+
 def test_defaults_and_reference_line():
     sys.path.insert(0, ROOT)
     import bench
