@@ -484,6 +484,21 @@ class A2avBench(Workload):
         moved = sum(int(x.sum()) for x in rc)
         return 4 * size * moved, dt, "the exchange with capacity %d rows per pair (counts scaled)" % mr
 
+    def oracle_parity(self, rows):
+        """The whole exchange on the host (a row copy per pair: seconds, and a
+        second set of target windows in host memory) against the resident
+        targets, sentinel rows included, and recv counts."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        tg = [np.full((tr, size), c["sentinel"], dtype=np.uint16) for _ in range(n)]
+        rc = [np.zeros(n, dtype=np.int32) for _ in range(n)]
+        sc = [np.ascontiguousarray(x, dtype=np.int32) for x in self.sc]
+        oracle.all_to_all_v(self.host, tg, sc, rc, tr, size, 2)
+        return _exchange_parity(self.d_tg, tg, "all %d target windows and recv counts" % n,
+                                self.d_rc, rc)
+
     def oracle_rows_per_second(self):
         nb, dt, _ = self.oracle_sample(16)
         return 16.0 / max(dt, 1e-9)
@@ -762,6 +777,28 @@ class PairsBench(A2avBench):
         moved = sum(int(x.sum()) for x in rc)
         return 6 * size * moved, dt, "the kAdd combine with capacity %d rows per pair (counts scaled)" % mr
 
+    def oracle_parity(self, rows):
+        """The whole operation on the host against the resident outputs, bit
+        for bit. The combine's windows come from the oracle's own dispatch of
+        the same inputs and counts, and it adds into copies of the prior
+        outputs (the resident outputs are restored before every step)."""
+        import numpy as np
+        import oracle
+        c = self.cfg
+        n, tr, size = c["nranks"], c["target_rows"], c["size"]
+        if self.op == "all_to_all":
+            tg = [np.full((tr, size), c["sentinel"], dtype=np.uint16) for _ in range(n)]
+            oracle.all_to_all(self.host, tg, tr, size, 2)
+            return _exchange_parity(self.d_tg, tg, "all %d target windows" % n)
+        win = [np.full((tr, size), c["sentinel"], dtype=np.uint16) for _ in range(n)]
+        rc = [np.zeros(n, dtype=np.int32) for _ in range(n)]
+        sc = [np.ascontiguousarray(x, dtype=np.int32) for x in self.sc]
+        oracle.all_to_all_v(self.host, win, sc, rc, tr, size, 2)
+        outs = [o.copy() for o in self.out_host]
+        oracle.all_to_all_v_combine(win, outs, rc, tr, size, oracle.ATOMIC_ADD, oracle.BF16)
+        del win
+        return _exchange_parity(self.d_out, outs, "all %d output windows" % n)
+
 
 class BarrierBench(Workload):
     """The credit barrier among N ranks simulated on the GPU: one launch of G
@@ -894,6 +931,20 @@ def _windows_parity(dev_windows, want, rows, total_rows):
            if not np.array_equal(np.ascontiguousarray(d[:rows].cpu().numpy()).view(np.uint8), w.view(np.uint8))]
     return {"rows": "0..%d of %d" % (rows - 1, total_rows),
             "result": "bit-exact" if not bad else "MISMATCH in windows " + ", ".join(map(str, bad))}
+
+
+def _exchange_parity(dev_out, want, what, dev_counts=None, want_counts=None):
+    """Whole resident output windows (and counts) against the oracle's, bit
+    for bit, one window at a time."""
+    import numpy as np
+    bad = []
+    for d, (t, w) in enumerate(zip(dev_out, want)):
+        got = np.ascontiguousarray(t.cpu().numpy()).view(np.uint8)
+        if not np.array_equal(got, w.view(np.uint8)):
+            bad.append(d)
+        elif dev_counts is not None and not np.array_equal(dev_counts[d].cpu().numpy(), want_counts[d]):
+            bad.append(d)
+    return {"rows": what, "result": "bit-exact" if not bad else "MISMATCH in windows " + ", ".join(map(str, bad))}
 
 
 def _pin(h):

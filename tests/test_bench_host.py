@@ -142,6 +142,40 @@ def test_window_samples_leave_the_inputs_alone(name):
     assert all(np.array_equal(a, b) for a, b in zip(before, wl.host))
 
 
+@pytest.mark.parametrize("name", ["a2av", "a2av_sparse", "all_to_all", "combine"])
+def test_exchange_parity_leg(name):
+    """The exchanges' parity check on host stand-ins for the resident outputs
+    (small windows stand in for the 16 x 24576 x 7168 ones): the oracle's own
+    result passes, one changed element fails."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    wl = bench.make_workload(name, 1)
+    wl.cfg = dict(wl.cfg, nranks=3, size=8, target_rows=12)
+    wl.setup_host()
+    c = wl.cfg
+    n, tr, size = 3, 12, 8
+    sc = [np.ascontiguousarray(x, dtype=np.int32) for x in wl.sc]
+    tg = [np.full((tr, size), c["sentinel"], dtype=np.uint16) for _ in range(n)]
+    rc = [np.zeros(n, dtype=np.int32) for _ in range(n)]
+    if name == "all_to_all":
+        oracle.all_to_all(wl.host, tg, tr, size, 2)
+    else:
+        oracle.all_to_all_v(wl.host, tg, sc, rc, tr, size, 2)
+    wl.d_tg = [torch.from_numpy(t.view(np.int16).copy()) for t in tg]
+    wl.d_rc = [torch.from_numpy(r.copy()) for r in rc]
+    if name == "combine":
+        outs = [o.copy() for o in wl.out_host]
+        oracle.all_to_all_v_combine(tg, outs, rc, tr, size, oracle.ATOMIC_ADD, oracle.BF16)
+        wl.d_out = [torch.from_numpy(o.view(np.int16).copy()) for o in outs]
+    assert wl.oracle_parity(0)["result"] == "bit-exact"
+    changed = wl.d_out if name == "combine" else wl.d_tg
+    changed[1][tr - 1, size - 1] ^= 1
+    assert wl.oracle_parity(0)["result"] == "MISMATCH in windows 1"
+
+
 def test_windows_parity_helper():
     import numpy as np
     import torch
