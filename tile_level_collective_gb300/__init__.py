@@ -106,7 +106,9 @@ def _addr(x):
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()          # a torch tensor
+    return x.ctypes.data             # a numpy array (host memory: the host credit barrier)
 
 
 def _stream(stream):
@@ -218,7 +220,8 @@ def ptoc_credit_barrier(signals, local_ranks, generations, timeout_ns, status, s
 
 def ptoc_credit_barrier_host(signals, rank, generations, timeout_ns, status, check=True):
     """Rank `rank`'s part of one host credit-barrier call, on the calling
-    thread. `signals` and `status` are HOST addresses (ints) or CPU tensors.
+    thread. `signals` and `status` are HOST memory: addresses (ints), CPU
+    tensors or numpy arrays.
     ctypes releases the GIL for the call, so ranks on Python threads run
     concurrently."""
     g, keep = _group(signals)
