@@ -12,7 +12,9 @@ HBM before timing; before every step L2 is flushed outside the timed events
 (a 256 MiB buffer is written, then read back, which leaves L2 cold and clean:
 no dirty flush lines for the timed kernels to write back). Other workloads
 (the parity configurations) can be timed with --workload for the per-kernel
-evidence.
+evidence. After the timed steps the CPU-baseline leg times the oracle on a
+bounded sample of the workload and then, untimed, compares the resident
+run's results with the oracle's (cpu_baseline.parity, bit for bit).
 
 --impl reference times the CPU oracle on the host's CPU cores (the only
 other implementation there is), on a bounded sample of the same workload per
