@@ -11,8 +11,9 @@
  *   [TR]  "CANN PTO-ISA TREDUCE 指令详解" (TREDUCE instruction explained,
  *         lpnh.cn news 2291107), sections 1 to 8 (一..八).
  *   [DO]  "Distributed Operators (N6)", pypto.ai dev/distributed_ops:
- *         the op table (Overview), "ABI enums", "pld.tensor.all_to_all_v",
- *         "pld.tensor.allreduce".
+ *         the op table (Overview), "ABI enums", "Barrier-signal protocol",
+ *         "pld.tensor.all_to_all_v", "pld.tensor.allreduce",
+ *         "pld.tensor.put", "pld.tile.remote_store".
  *
  * Readings taken where the pages are silent or garbled are stated beside the
  * code that takes them. Every function here is pinned by tests that do not
