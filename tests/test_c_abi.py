@@ -1,6 +1,7 @@
 """The C ABI from C: include/ptoc.h compiles as C99 and as C++ (CPU), and a
 plain C program that owns its buffers (cudaMalloc) drives the library and
-checks closed-form results (GPU)."""
+checks closed-form results (GPU); a plain C program runs the host credit
+barrier with POSIX threads as ranks (CPU)."""
 import os
 import shutil
 import subprocess
@@ -49,3 +50,19 @@ def test_plain_c_caller(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "abi_check: ok" in r.stdout
+
+
+def test_plain_c_host_barrier(tmp_path):
+    """ptoc_credit_barrier_host from C with POSIX threads as ranks (no GPU):
+    complete calls self-clear, an absent rank leaves the protocol's credits."""
+    exe = tmp_path / "host_barrier_check"
+    libdir = os.path.dirname(P.LIB_PATH)
+    cmd = ["gcc", "-std=c11", "-O1", "-pthread", "-o", str(exe),
+           os.path.join(ROOT, "tests", "c", "host_barrier_check.c"),
+           "-I", os.path.join(ROOT, "include"), "-I", cuda_include(), "-L", libdir, "-lptoc",
+           "-Wl,-rpath," + libdir]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "host barrier: ok" in r.stdout
