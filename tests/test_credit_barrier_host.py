@@ -132,3 +132,26 @@ def test_host_barrier_rejects():
     assert B([win[0], win[0] + 4, win[2], win[3]], 0, 1, 10 ** 9, ST, check=False) == P.ERR_ALIAS
     assert B(win, 0, 1, 10 ** 9, win[3] + 4, check=False) == P.ERR_ALIAS      # status over a window
     assert np.all(sig == 0) and np.all(out == 0)                               # nothing ran
+
+
+def test_threads_random_presence_against_the_oracle():
+    """Seeded random rank counts, generations and presence patterns: the
+    statuses and the cells the threads leave equal the oracle's (with a rank
+    absent every present rank gives up in generation 1, whatever the
+    interleaving; with all present everything clears)."""
+    rng = np.random.default_rng(11)
+    for _ in range(24):
+        n = int(rng.integers(1, 13))
+        g = int(rng.integers(1, 6))
+        present = (rng.random(n) < 0.8).astype(np.int32)
+        if not present.any():
+            present[int(rng.integers(n))] = 1
+        sig = np.zeros((n, n), np.int32)
+        timeout = 20 * 10 ** 9 if present.all() else 30 * 10 ** 6
+        st = run_threads(sig, [r for r in range(n) if present[r]], g, timeout)
+        want_sig = np.zeros((n, n), np.int32)
+        want_st = oracle.credit_barrier(n, g, present, want_sig)
+        assert np.array_equal(sig, want_sig), (n, g, present)
+        for r in range(n):
+            if present[r]:
+                assert st[r] == want_st[r], (n, g, present, r)
