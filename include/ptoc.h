@@ -15,7 +15,8 @@
  *
  * Conventions shared by every entry point
  *   - Every data pointer is a DEVICE pointer on the calling thread's current
- *     CUDA device. Pointer arrays (ptoc_group.tensors, send_counts,
+ *     CUDA device, except in ptoc_credit_barrier_host, whose windows and
+ *     status are host memory. Pointer arrays (ptoc_group.tensors, send_counts,
  *     recv_counts) are HOST arrays of device pointers; they are read during
  *     the call and copied into kernel parameters, so the caller may free or
  *     reuse them as soon as the call returns.
@@ -27,7 +28,8 @@
  *     it becomes a graph memory node), zeroed, and freed in stream order
  *     after the call's kernel. An allocation failure is PTOC_ERR_CUDA.
  *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
- *     stream). Completion is observed through the stream; results must not be
+ *     stream); ptoc_credit_barrier_host, which has no stream, runs on the
+ *     calling thread and returns when that rank is done. Completion is observed through the stream; results must not be
  *     read, and inputs must not be modified, before the stream reaches them.
  *   - Layout: a "slice" is row-major with a row pitch of `ld` ELEMENTS
  *     (ld >= cols). Element (i, j) is at offset i*ld + j. The footprint the
