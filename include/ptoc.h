@@ -28,9 +28,10 @@
  *     it becomes a graph memory node), zeroed, and freed in stream order
  *     after the call's kernel. An allocation failure is PTOC_ERR_CUDA.
  *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
- *     stream); ptoc_credit_barrier_host, which has no stream, runs on the
- *     calling thread and returns when that rank is done. Completion is observed through the stream; results must not be
- *     read, and inputs must not be modified, before the stream reaches them.
+ *     stream). Completion is observed through the stream; results must not
+ *     be read, and inputs must not be modified, before the stream reaches
+ *     them. ptoc_credit_barrier_host, which has no stream, runs on the
+ *     calling thread and returns when that rank is done.
  *   - Layout: a "slice" is row-major with a row pitch of `ld` ELEMENTS
  *     (ld >= cols). Element (i, j) is at offset i*ld + j. The footprint the
  *     library may touch is (rows-1)*ld + cols elements from the base pointer.
