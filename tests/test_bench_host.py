@@ -240,3 +240,15 @@ def test_traffic_source_lists_exist():
     device = {os.path.relpath(f, ROOT) for f in glob.glob(os.path.join(csrc, "*"))
               if f.endswith((".cuh", ".h")) or os.path.basename(f).startswith(("reduce_", "movement"))}
     assert device <= listed, device - listed
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm's rank 0 alone times the oracle and
+    prints the line; the other ranks exit 0 without work or output."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "2", "--warmup", "1", "--reference-seconds", "1",
+                          "--workload", "treduce_small"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == ""
