@@ -107,16 +107,22 @@ def test_reduce_scatter_and_allgather_reject():
     assert P.ptoc_allgather([A], 64, 64, 64, P.F16, stream=0, check=False) == P.OK   # one rank: nothing to move
 
 
+A2AV_CALL = {"call": P.ptoc_all_to_all_v}
+
+
 def a2av(inputs=None, targets=None, sc=None, rc=None, tr_=64, size=16, dt=P.BF16):
     n = 4
     inputs = srcs(n) if inputs is None else inputs
     targets = srcs(n, base=A + 8 * 64 * MB) if targets is None else targets
     sc = [A + 16 * 64 * MB + 256 * r for r in range(n)] if sc is None else sc
     rc = [A + 17 * 64 * MB + 256 * r for r in range(n)] if rc is None else rc
-    return P.ptoc_all_to_all_v(inputs, targets, sc, rc, tr_, size, dt, stream=0, check=False)
+    return A2AV_CALL["call"](inputs, targets, sc, rc, tr_, size, dt, stream=0, check=False)
 
 
-def test_all_to_all_v_rejects():
+@pytest.mark.parametrize("call", ["ptoc_all_to_all_v", "ptoc_all_to_all_v_noalloc"])
+def test_all_to_all_v_rejects(call, monkeypatch):
+    """The same checks guard the allocating and the no-allocation entry point."""
+    monkeypatch.setitem(A2AV_CALL, "call", getattr(P, call))
     assert a2av(targets=srcs(3, base=A + 8 * 64 * MB)) == P.ERR_INVALID_ARG        # N mismatch
     assert a2av(sc=[A + 16 * 64 * MB, 0, A + 16 * 64 * MB + 512, A + 16 * 64 * MB + 768]) == P.ERR_INVALID_ARG
     assert a2av(rc=[A + 17 * 64 * MB + 2, A + 17 * 64 * MB + 256, A + 17 * 64 * MB + 512,
@@ -195,5 +201,7 @@ def test_device_count_exchanges_reject_int32_tile_overflow():
     sc = [B + 2 * n * S + 256 * r for r in range(n)]
     rc = [B + 2 * n * S + (1 << 20) + 256 * r for r in range(n)]
     assert P.ptoc_all_to_all_v(ins, tgs, sc, rc, tr_, size, P.BF16, stream=0, check=False) == P.ERR_UNSUPPORTED
+    assert P.ptoc_all_to_all_v_noalloc(ins, tgs, sc, rc, tr_, size, P.BF16, stream=0,
+                                       check=False) == P.ERR_UNSUPPORTED
     assert P.ptoc_all_to_all_v_combine(ins, tgs, rc, tr_, size, P.ATOMIC_ADD, P.BF16, stream=0,
                                        check=False) == P.ERR_UNSUPPORTED
