@@ -547,7 +547,7 @@ static ptoc_status a2av_setup(const ptoc_group* inputs, const ptoc_group* target
     // Outputs (targets, recv_counts) must not overlap anything (the page
     // requires the five operands to be pairwise-distinct allocations); inputs
     // may share memory.
-    Span writes[2 * kMaxRanks], reads[2 * kMaxRanks];
+    Span writes[2 * kMaxRanks] = {}, reads[2 * kMaxRanks] = {};
     for (int r = 0; r < n; ++r) {
         writes[r] = Span{targets->tensors[r], (uintptr_t)fp};
         writes[n + r] = Span{recv_counts[r], (uintptr_t)n * 4u};
@@ -645,7 +645,7 @@ extern "C" ptoc_status ptoc_all_to_all(const ptoc_group* inputs, const ptoc_grou
     if (fp < 0) return PTOC_ERR_INVALID_ARG;
     for (int r = 0; r < n; ++r)
         if (!aligned(inputs->tensors[r], eb) || !aligned(targets->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
-    Span writes[kMaxRanks], reads[kMaxRanks];
+    Span writes[kMaxRanks] = {}, reads[kMaxRanks] = {};
     for (int r = 0; r < n; ++r) {
         writes[r] = Span{targets->tensors[r], (uintptr_t)fp};
         reads[r] = Span{inputs->tensors[r], (uintptr_t)fp};
@@ -689,7 +689,7 @@ extern "C" ptoc_status ptoc_all_to_all_v_combine(const ptoc_group* windows, cons
         if (!recv_counts[r] || !aligned(recv_counts[r], 4)) return PTOC_ERR_INVALID_ARG;
         if (!aligned(windows->tensors[r], eb) || !aligned(outputs->tensors[r], eb)) return PTOC_ERR_INVALID_ARG;
     }
-    Span writes[kMaxRanks], reads[2 * kMaxRanks];
+    Span writes[kMaxRanks] = {}, reads[2 * kMaxRanks] = {};
     for (int r = 0; r < n; ++r) {
         writes[r] = Span{outputs->tensors[r], (uintptr_t)fp};
         reads[r] = Span{windows->tensors[r], (uintptr_t)fp};
@@ -735,7 +735,7 @@ extern "C" ptoc_status ptoc_credit_barrier(const ptoc_group* signals, const int3
     }
     for (int r = 0; r < n; ++r)
         if (!aligned(signals->tensors[r], 4)) return PTOC_ERR_INVALID_ARG;
-    Span writes[kMaxRanks + 1];
+    Span writes[kMaxRanks + 1] = {};
     for (int r = 0; r < n; ++r) writes[r] = Span{signals->tensors[r], (uintptr_t)n * 4u};
     writes[n] = Span{status, (uintptr_t)n_local * 4u};
     st = check_disjoint_outputs(writes, n + 1, nullptr, 0);
