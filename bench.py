@@ -3,18 +3,24 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
 
-Default workload: TREDUCE over 8 ranks of bf16 [4096, 4096] with a 4000 x 4000
-valid box inside NaN-sentinel padding, N(0, 1) values; one step = Sum, Max and
-Min (three launches). Metric: effective HBM GB/s = (N + 1) * bytes/elem *
-valid elements per launch, summed over the step, divided by the step's device
-time. Inputs are generated on the host by the seeded generator and resident in
-HBM before timing; before every step L2 is flushed outside the timed events
-(a 256 MiB buffer is written, then read back, which leaves L2 cold and clean:
-no dirty flush lines for the timed kernels to write back). Other workloads
-(the parity configurations) can be timed with --workload for the per-kernel
+Default workload: TREDUCE over 8 ranks of [16384, 8192] 4-byte elements, the
+largest TREDUCE case: f32 Sum over U[-1e3, 1e3] inputs and the int32 Max
+variant over U[-2^30, 2^30] inputs, each over its own sources (8 x 512 MiB);
+one step = the two launches. Metric: effective HBM GB/s = (N + 1) *
+bytes/elem * valid elements per launch, summed over the step, divided by the
+step's device time. Inputs are generated on the host by the seeded generator
+and resident in HBM before timing; before every step L2 is flushed outside the
+timed events (a 256 MiB buffer is written, then read back, which leaves L2
+cold and clean: no dirty flush lines for the timed kernels to write back), and
+each launch reads 4 GiB besides, far more than L2. The K-step block is timed
+again, back to back, until the timed region spans half a second, so that the
+clock record samples it; every timed step counts. Other workloads (the bf16
+4096 x 4096 case with its 4000 x 4000 valid box as `--workload treduce`, and
+the parity configurations) can be timed with --workload for the per-kernel
 evidence. After the timed steps the CPU-baseline leg times the oracle on a
-bounded sample of the workload and then, untimed, compares the resident
-run's results with the oracle's (cpu_baseline.parity, bit for bit).
+bounded sample of the workload and then, untimed, compares the resident run's
+results with the oracle's (cpu_baseline.parity, bit for bit; every element
+for the TREDUCE workloads).
 
 --impl reference times the CPU oracle on the host's CPU cores (the only
 other implementation there is), on a bounded sample of the same workload per
@@ -224,6 +230,49 @@ class TreduceBench(Workload):
         return {"rows": "0..%d of %d" % (rows - 1, w.valid_rows), "ops": list(w.ops),
                 "result": "bit-exact" if not bad else "MISMATCH in " + ", ".join(bad)}
 
+    def max_rows(self):
+        return self.w.valid_rows
+
+    def oracle_parity_all(self, threads=None):
+        """Every element of the resident run's results against the oracle on
+        the same host inputs, bit for bit: the whole valid box of every op,
+        and the padding around it still holding its sentinel. The oracle runs
+        on contiguous row slices, one host thread each (a split run equals
+        one call, byte for byte)."""
+        import numpy as np
+        w = self.w
+        threads = threads or os.cpu_count() or 1
+        bad = []
+        for i, op in enumerate(w.ops):
+            want = self.oracle_rows_threaded(0, w.valid_rows, op, threads)
+            got = np.ascontiguousarray(self.dsts[i].cpu().numpy()).view(want.dtype)
+            if not np.array_equal(got.view(np.uint8), want.view(np.uint8)):
+                bad.append(op)
+        return {"rows": "all %d of %d (every element, padding included)" % (w.valid_rows, w.rows),
+                "ops": list(w.ops), "result": "bit-exact" if not bad else "MISMATCH in " + ", ".join(bad)}
+
+    def oracle_rows_threaded(self, lo, hi, op, threads):
+        """The oracle's full dst (padding as initialised) for valid rows
+        [lo, hi) of one op, split into `threads` contiguous row slices on as
+        many host threads; rows outside [lo, hi) keep the padding."""
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+        w = self.w
+        out = self.dst_init.copy()
+        code = {"f32": oracle.F32, "bf16": oracle.BF16, "f16": oracle.F16, "i32": oracle.I32}[self.storage]
+        code_op = {"sum": oracle.SUM, "max": oracle.MAX, "min": oracle.MIN}[op]
+        n = hi - lo
+        bounds = [lo + n * t // threads for t in range(threads + 1)]
+
+        def part(t):
+            a, b = bounds[t], bounds[t + 1]
+            if b > a:
+                oracle.treduce([h[a:b] for h in self.host], out[a:b], b - a, w.valid_cols, w.ld, code_op, code)
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(part, range(threads)))
+        return out
+
     def oracle_sample_threaded(self, rows, threads):
         """The same oracle call on `rows` rows, the rows split into `threads`
         contiguous slices run on as many host threads (ctypes releases the
@@ -250,6 +299,112 @@ class TreduceBench(Workload):
             dt = time.perf_counter() - t0
         nbytes = (w.nranks + 1) * w.elem_bytes * rows * w.valid_cols * len(w.ops)
         return nbytes, dt, out
+
+
+class TreducePairBench(Workload):
+    """The two TREDUCE launches of one 8-rank [16384, 8192] case: f32 Sum over
+    U[-1e3, 1e3] inputs and the int32 Max variant over U[-2^30, 2^30] inputs
+    (each with its own 8 x 512 MiB of sources and its own dst), one launch of
+    each per step. Every figure is the sum over the two parts."""
+    pipelined_e2e = True
+
+    def __init__(self, parts):
+        self.parts = parts
+        w = parts[0].w
+        assert all(p.w.algorithmic_bytes() == w.algorithmic_bytes() and len(p.w.ops) == 1 for p in parts)
+        self.name = "treduce_n8_16384x8192_f32sum_i32max"
+        self.kernel = "reduce_kernel<f32, Sum> and reduce_kernel<i32, Max> (one block per tile)"
+        self.dtype_compute = "+".join(p.dtype_compute for p in parts)
+
+    def bytes_per_launch(self):
+        return self.parts[0].bytes_per_launch()
+
+    def launches_per_step(self):
+        return len(self.parts)
+
+    def bytes_per_step(self):
+        return sum(p.bytes_per_step() for p in self.parts)
+
+    def max_rows(self):
+        return self.parts[0].w.valid_rows
+
+    def setup_host(self):
+        for p in self.parts:
+            p.setup_host()
+
+    def setup_device(self, dev):
+        for p in self.parts:
+            p.setup_device(dev)
+
+    def launch(self, i, srcs=None, dst=None):
+        self.parts[i].launch(0, srcs, dst)
+
+    def setup_e2e(self, dev):
+        for p in self.parts:
+            p.setup_e2e(dev)
+
+    def e2e_upload(self, b):
+        for p in self.parts:
+            p.e2e_upload(b)
+
+    def e2e_compute(self, b):
+        for p in self.parts:
+            p.e2e_compute(b)
+
+    def e2e_download(self, b):
+        for p in self.parts:
+            p.e2e_download(b)
+
+    def e2e_verify(self, b):
+        for p in self.parts:
+            p.e2e_verify(b)
+
+    def h2d_bytes(self):
+        return sum(p.h2d_bytes() for p in self.parts)
+
+    def d2h_bytes(self):
+        return sum(p.d2h_bytes() for p in self.parts)
+
+    def config(self):
+        w = self.parts[0].w
+        return {"workload": self.name, "op": "TREDUCE", "nranks": w.nranks,
+                "storage_dtype": "+".join(p.storage for p in self.parts),
+                "shape": [w.rows, w.cols], "ld": w.ld, "valid": [w.valid_rows, w.valid_cols],
+                "ops": ["%s %s" % (p.storage, p.w.ops[0]) for p in self.parts], "root": w.root,
+                "values": "; ".join("%s %s[%s, %s]" % ((p.storage,) + tuple(p.w.dist)) for p in self.parts),
+                "seed": "1234 + rank (SplitMix64, counter-based)",
+                "step": "%d TREDUCE launches (%s), each over its own 8 sources" % (
+                    len(self.parts), ", ".join("%s %s" % (p.storage, p.w.ops[0]) for p in self.parts)),
+                "bytes_per_step": self.bytes_per_step(),
+                "l2": L2_NOTE + "; each launch also reads 4 GiB, 33x L2"}
+
+    def oracle_sample(self, rows):
+        nb_tot, dt_tot, descs = 0, 0.0, []
+        for p in self.parts:
+            nb, dt, desc = p.oracle_sample(rows)
+            nb_tot, dt_tot = nb_tot + nb, dt_tot + dt
+            descs.append("%s: %s" % (p.storage, desc))
+        return nb_tot, dt_tot, "; ".join(descs)
+
+    def oracle_rows_per_second(self):
+        return 1.0 / sum(1.0 / p.oracle_rows_per_second() for p in self.parts)
+
+    def oracle_parity(self, rows):
+        return self.oracle_parity_all()
+
+    def oracle_parity_all(self, threads=None):
+        res = [p.oracle_parity_all(threads) for p in self.parts]
+        bad = [p.storage + " " + r["result"] for p, r in zip(self.parts, res) if r["result"] != "bit-exact"]
+        return {"rows": res[0]["rows"], "ops": ["%s %s" % (p.storage, p.w.ops[0]) for p in self.parts],
+                "result": "bit-exact" if not bad else "; ".join(bad)}
+
+    def oracle_sample_threaded(self, rows, threads):
+        nb_tot, dt_tot, outs = 0, 0.0, []
+        for p in self.parts:
+            nb, dt, out = p.oracle_sample_threaded(rows, threads)
+            nb_tot, dt_tot = nb_tot + nb, dt_tot + dt
+            outs.append(out)
+        return nb_tot, dt_tot, outs
 
 
 class RsAgBench(Workload):
@@ -854,6 +1009,9 @@ def make_workload(name, rows_div=1):
         wl = TreduceBench(synth.treduce_f32_n8_16384x8192(), "f32")
     elif name == "treduce_i32":
         wl = TreduceBench(synth.treduce_i32_n8_16384x8192(), "i32")
+    elif name == "treduce_16384x8192":
+        wl = TreducePairBench([TreduceBench(synth.treduce_f32_n8_16384x8192(), "f32"),
+                               TreduceBench(synth.treduce_i32_n8_16384x8192(), "i32")])
     elif name == "rs_ag":
         wl = RsAgBench()
     elif name == "a2av":
@@ -869,11 +1027,14 @@ def make_workload(name, rows_div=1):
     else:
         raise SystemExit("unknown workload %s" % name)
     if rows_div > 1:
-        if isinstance(wl, TreduceBench):
-            w = wl.w
-            w.rows, w.valid_rows = w.rows // rows_div, w.valid_rows // rows_div
-            w.name += "_rows_div%d" % rows_div
-            wl.name = w.name
+        if isinstance(wl, (TreduceBench, TreducePairBench)):
+            for part in getattr(wl, "parts", [wl]):
+                w = part.w
+                w.rows, w.valid_rows = w.rows // rows_div, w.valid_rows // rows_div
+                w.name += "_rows_div%d" % rows_div
+                part.name = w.name
+            if isinstance(wl, TreducePairBench):
+                wl.name += "_rows_div%d" % rows_div
         else:
             wl.cfg = dict(wl.cfg)
             key = "rows" if isinstance(wl, (RsAgBench, WindowOpBench)) else "target_rows"
@@ -1091,9 +1252,14 @@ def cpu_baseline(wl, budget_s):
         nb_tot, dt_tot, reps = nb_tot + nb, dt_tot + dt, reps + 1
     line = {"value": nb_tot / dt_tot / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%s, %d repetition(s)" % (desc, reps), "seconds": round(dt_tot, 3)}
-    if hasattr(wl, "oracle_parity"):
+    if hasattr(wl, "oracle_parity_all"):
+        # untimed: every element of the resident run's results against the
+        # oracle (row slices on every host core)
+        line["parity"] = wl.oracle_parity_all()
+    elif hasattr(wl, "oracle_parity"):
         # the same sample, untimed, against the resident run's results
         line["parity"] = wl.oracle_parity(rows)
+    if "parity" in line:
         if line["parity"]["result"] != "bit-exact":
             print("bench: results differ from the oracle: %s" % line["parity"], file=sys.stderr)
     if hasattr(wl, "oracle_sample_threaded"):
@@ -1106,7 +1272,7 @@ def cpu_baseline(wl, budget_s):
             nb_t, dt_t, reps_t = nb_t + nb, dt_t + dt, reps_t + 1
         line["all_cores"] = {"value": nb_t / dt_t / 1e9, "cores": threads, "seconds": round(dt_t, 3),
                              "sample": "the first %d rows, split into %d row slices on as many threads, "
-                             "%d repetition(s)" % (min(n_rows, wl.w.valid_rows), threads, reps_t)}
+                             "%d repetition(s)" % (min(n_rows, wl.max_rows()), threads, reps_t)}
     return line
 
 
@@ -1141,34 +1307,49 @@ def run_ours(args):
     if sampler:
         time.sleep(0.6)          # let the sampler start before the timed region
     nev = nl if wl.per_launch_timing else 1
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nev)]
-          for _ in range(args.steps)]
+
+    def timed_block():
+        """K steps, each bracketed by CUDA events on the launching stream;
+        returns the events."""
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nev)] for _ in range(args.steps)]
+        for k in range(args.steps):
+            wl.prepare()
+            flush(k)
+            if wl.per_launch_timing:
+                for i in range(nl):
+                    ev[k][i][0].record(stream)
+                    wl.launch(i)
+                    ev[k][i][1].record(stream)
+            else:
+                ev[k][0][0].record(stream)
+                for i in range(nl):
+                    wl.launch(i)
+                ev[k][0][1].record(stream)
+        torch.cuda.synchronize()
+        return ev
+
+    # The K-step block is timed again, back to back, until the timed region
+    # spans --min-timed-seconds, so that the clock sampler sees it several
+    # times; every timed step counts.
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    for k in range(args.steps):
-        wl.prepare()
-        flush(k)
-        if wl.per_launch_timing:
-            for i in range(nl):
-                ev[k][i][0].record(stream)
-                wl.launch(i)
-                ev[k][i][1].record(stream)
-        else:
-            ev[k][0][0].record(stream)
-            for i in range(nl):
-                wl.launch(i)
-            ev[k][0][1].record(stream)
-    torch.cuda.synchronize()
+    blocks = []
+    while not blocks or time.time() - t0 < args.min_timed_seconds:
+        blocks.append(timed_block())
     barrier()
     t1 = time.time()
     if sampler:
         sampler.stop()
-    timed = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(nev)] for k in range(args.steps)]
+    timed = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(nev)] for ev in blocks
+             for k in range(args.steps)]
     # a step = its launches on the stream (the flush between steps excluded)
     step_ms = [sum(x) for x in timed]
-    ms_local = sum(step_ms) / args.steps
+    ms_local = sum(step_ms) / len(step_ms)
     ms, value = aggregate(ms_local, wl.bytes_per_step(), world, dev)
+    block_gbs = sorted(wl.bytes_per_step() * args.steps / (sum(step_ms[b * args.steps:(b + 1) * args.steps])
+                                                           / 1e3) / 1e9 for b in range(len(blocks)))
 
     # roofline of the dominant kernel: launch 0 when launches are timed one by
     # one, else the step's average launch (all of one kernel family)
@@ -1187,7 +1368,7 @@ def run_ours(args):
                               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
                               "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
                               "dtype": "i32", "data": "synthetic", "config": wl.config(),
-                              "roofline": None, "e2e": None, "gpu_launches": args.steps,
+                              "roofline": None, "e2e": None, "gpu_launches": args.steps * len(blocks),
                               "clocks": sampler.summary(t0, t1) if sampler else None}), flush=True)
         return
 
@@ -1199,7 +1380,7 @@ def run_ours(args):
     if rank != 0:
         return
     line = build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl,
-                      sampler.summary(t0, t1) if sampler else None)
+                      sampler.summary(t0, t1) if sampler else None, len(blocks), block_gbs, t1 - t0)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -1262,13 +1443,20 @@ def run_e2e(wl, args, dev, stream, world, barrier):
     return run_e2e_pipelined(wl, args, dev, world, barrier)
 
 
-def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl, clocks):
+def line_config(wl, world):
+    """The `config` of both arms' lines (identical for the same workload and
+    rank count)."""
+    return dict(wl.config(), parallelism="replicas" if world > 1 else "single GPU")
+
+
+def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl, clocks,
+               nblocks=1, block_gbs=None, timed_s=None):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype_compute, "data": "synthetic (seeded SplitMix64, generated on the host)",
-        "config": dict(wl.config(), parallelism="replicas" if world > 1 else "single GPU"),
+        "config": line_config(wl, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": wl.kernel,
                      "bytes_per_launch": wl.bytes_per_launch(), "avg_launch_ms": round(avg0, 6),
@@ -1280,10 +1468,17 @@ def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traff
                      "pinned host copy of its results; double-buffered on three streams (upload of step k "
                      "overlaps compute and download of step k-1); the last results checked against the "
                      "resident run")},
-        "gpu_launches": nl * args.steps,
+        "gpu_launches": nl * args.steps * nblocks,
         "timing": ("CUDA events around each launch" if wl.per_launch_timing else
                    "CUDA events around each step; its %d launches run back to back (programmatic "
-                   "dependent launch lets each overlap the previous one's tail)" % nl),
+                   "dependent launch lets each overlap the previous one's tail)" % nl)
+        + ("; the %d-step block timed %d times back to back (%.2f s of timed region, so that the clock "
+           "record samples it), value over all %d timed steps" % (args.steps, nblocks, timed_s or 0.0,
+                                                                  args.steps * nblocks)),
+        "timed_blocks": nblocks,
+        "block_gbs": None if not block_gbs else {"min": round(block_gbs[0], 2),
+                                                 "median": round(statistics.median(block_gbs), 2),
+                                                 "max": round(block_gbs[-1], 2)},
         "clocks": clocks,
     }
     return line
@@ -1315,8 +1510,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt_tot / args.steps * 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype_compute, "data": "synthetic",
-        "config": wl.config(),
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype_compute,
+        "data": "synthetic (seeded SplitMix64, generated on the host)",
+        "config": line_config(wl, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1330,13 +1526,16 @@ def parse(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="treduce",
-                    choices=["treduce", "treduce_bf16", "treduce_small", "treduce_f32", "treduce_i32",
+    ap.add_argument("--workload", default="treduce_16384x8192",
+                    choices=["treduce_16384x8192", "treduce", "treduce_bf16", "treduce_small", "treduce_f32",
+                             "treduce_i32",
                              "rs_ag", "a2av", "a2av_sparse", "allreduce", "broadcast", "all_to_all", "combine",
                              "barrier"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--min-timed-seconds", type=float, default=0.5,
+                    help="repeat the timed K-step block until the timed region spans this long")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiler runs)")

@@ -43,6 +43,30 @@
  *     round-to-nearest-even narrowing per output element; subnormals kept;
  *     Sum adds one rank at a time in the documented rank order (no fused or
  *     reassociated arithmetic). int32 Sum wraps modulo 2^32.
+ *   - Per-device state: the library caches, per device ordinal, the SM
+ *     count, the counter pool above and the address of the no-allocation
+ *     scratch block. They assume the device's primary context lives as long
+ *     as the process; after cudaDeviceReset they are stale, so do not call
+ *     the library on a device that has been reset.
+ *
+ * Environment switches (read at every call; results never depend on them)
+ *   PTOC_PDL=0           launch the data kernels as ordinary launches. By
+ *                        default they are programmatic dependent launches:
+ *                        a launch may begin while the previous kernel of the
+ *                        stream finishes, and waits for that kernel's
+ *                        completion and writes before it touches memory.
+ *                        Turning it off gives strict launch boundaries (for
+ *                        tools that time or replay kernels one by one).
+ *   PTOC_A2AV_UNROLL=4|16
+ *                        16-byte chunks per thread in one tile of the
+ *                        exchanges' copy kernel (ptoc_all_to_all_v, its
+ *                        no-allocation twin, ptoc_all_to_all and the
+ *                        PTOC_ATOMIC_NONE combine): 16 or 64 KiB tiles
+ *                        instead of the default 32 KiB (8 chunks), for
+ *                        16-byte-aligned rows (narrower vectors scale the
+ *                        tiles down in proportion). It trades
+ *                        scheduling granularity against per-tile overhead;
+ *                        any other value means the default.
  */
 #ifndef PTOC_H
 #define PTOC_H

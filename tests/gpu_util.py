@@ -1,6 +1,9 @@
 """Helpers of the GPU parity tests: guard-banded device buffers (so an
 out-of-bounds write shows up as a changed guard byte), host <-> device copies
 of raw encodings, and the oracle's dtype codes."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -70,3 +73,23 @@ def first_diff(got, want):
     return "%d elements differ, first at %s: got %s want %s" % (
         len(d), d[:3].tolist(), [hex(int(bits(got)[tuple(i)])) for i in d[:3]],
         [hex(int(bits(want)[tuple(i)])) for i in d[:3]]) if len(d) else "equal"
+
+
+def oracle_treduce_threaded(srcs, dst, valid_rows, valid_cols, ld, op, dtype, threads=None, root=0):
+    """oracle.treduce over contiguous row slices of the valid box, one host
+    thread each (ctypes releases the interpreter lock during a call). Each
+    element's result depends only on that element of every source, so the
+    split run writes exactly what one call writes (checked on the CPU in
+    test_oracle_split.py). Returns the first non-zero return code, else 0."""
+    threads = threads or os.cpu_count() or 1
+    bounds = [valid_rows * t // threads for t in range(threads + 1)]
+
+    def part(t):
+        a, b = bounds[t], bounds[t + 1]
+        if b <= a:
+            return 0
+        return oracle.treduce([s[a:b] for s in srcs], dst[a:b], b - a, valid_cols, ld, op, dtype, root)
+
+    with ThreadPoolExecutor(threads) as ex:
+        rcs = list(ex.map(part, range(threads)))
+    return next((rc for rc in rcs if rc != 0), 0)

@@ -192,7 +192,7 @@ def test_defaults_and_reference_line():
     sys.path.insert(0, ROOT)
     import bench
     a = bench.parse([])
-    assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours" and a.workload == "treduce"
+    assert a.gpus == 1 and a.warmup >= 3 and a.impl == "ours" and a.workload == "treduce_16384x8192"
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--steps", "2", "--warmup", "1", "--reference-seconds", "1",
                           "--workload", "treduce_small"],
@@ -204,6 +204,53 @@ def test_defaults_and_reference_line():
         assert key in line
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+    # the same config dict as the GPU arm's line for this workload at N = 1
+    assert line["config"] == bench.line_config(bench.make_workload("treduce_small"), 1)
+
+
+def test_default_workload_is_the_largest_treduce_case():
+    """The default step is the 8-rank [16384, 8192] TREDUCE: f32 Sum and the
+    int32 Max variant, one launch each, (N + 1) * 4 bytes per valid element."""
+    sys.path.insert(0, ROOT)
+    import bench
+    wl = bench.make_workload(bench.parse([]).workload)
+    assert wl.launches_per_step() == 2
+    assert [(p.storage, p.w.ops) for p in wl.parts] == [("f32", ["sum"]), ("i32", ["max"])]
+    for p in wl.parts:
+        w = p.w
+        assert (w.nranks, w.rows, w.cols, w.ld, w.valid_rows, w.valid_cols) == (8, 16384, 8192, 8192, 16384, 8192)
+    assert wl.bytes_per_launch() == 9 * 4 * 16384 * 8192
+    assert wl.bytes_per_step() == 2 * wl.bytes_per_launch()
+    cfg = bench.line_config(wl, 1)
+    assert cfg["workload"] == "treduce_n8_16384x8192_f32sum_i32max" and cfg["parallelism"] == "single GPU"
+
+
+def test_full_parity_leg_of_the_default_workload():
+    """The default workload's parity check compares every element of both
+    results with the oracle (row slices on threads): host stand-ins for the
+    resident results pass when they are the oracle's, and one changed
+    element in either part fails (rows divided by 512 stand in for the full
+    case)."""
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    wl = bench.make_workload("treduce_16384x8192", rows_div=512)
+    wl.setup_host()
+    for p in wl.parts:
+        w = p.w
+        p.dst_init = np.zeros((w.rows, w.ld), dtype=p.host[0].dtype)
+        want = p.dst_init.copy()
+        op = {"sum": oracle.SUM, "max": oracle.MAX}[w.ops[0]]
+        code = {"f32": oracle.F32, "i32": oracle.I32}[p.storage]
+        assert oracle.treduce(p.host, want, w.valid_rows, w.valid_cols, w.ld, op, code) == 0
+        p.dsts = [torch.from_numpy(want)]
+    got = wl.oracle_parity_all(threads=5)
+    assert got["result"] == "bit-exact" and got["rows"].startswith("all 32 of 32")
+    d = wl.parts[1].dsts[0]
+    d[31, 8191] += 1
+    assert wl.oracle_parity_all(threads=3)["result"] == "i32 MISMATCH in max"
 
 
 def test_threaded_oracle_sample_matches_one_call():

@@ -26,6 +26,7 @@ struct TraceRange {
     TraceRange& operator=(const TraceRange&) = delete;
 };
 
+// The documented switch PTOC_PDL=0 turns programmatic dependent launch off.
 bool programmatic_launch()
 {
     const char* e = getenv("PTOC_PDL");
@@ -158,8 +159,8 @@ uint32_t* zeroed_counter(cudaStream_t stream)
     return (uint32_t*)ptr;
 }
 
-// Chunks per thread per all_to_all_v tile: PTOC_A2AV_UNROLL=4|8|16 (A/B
-// switch for measurements; default 8, 32 KB tiles for 16-byte vectors).
+// Chunks per thread per tile of the exchanges' copy kernel: the documented
+// switch PTOC_A2AV_UNROLL=4|16, else 8 (32 KiB tiles for 16-byte vectors).
 int a2av_unroll()
 {
     const char* e = getenv("PTOC_A2AV_UNROLL");
@@ -593,7 +594,15 @@ extern "C" ptoc_status ptoc_all_to_all_v(const ptoc_group* inputs, const ptoc_gr
 constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
 
+namespace {
+
+// Per-device cache of the block's address. Like the other per-device caches
+// of the library (SM counts, the counter pool), it assumes the device's
+// primary context lives as long as the process: after a cudaDeviceReset the
+// cached values are stale.
 std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+}  // namespace
 
 // The scratch block's device address on the current device, looked up once
 // per device (with that device current).

@@ -91,8 +91,8 @@ cudaError_t launch_credit_barrier(const BarrierParams& p, cudaStream_t s);
 // Whether the data kernels are launched as programmatic dependent launches:
 // a launch may then overlap the tail of the previous kernel of the stream,
 // and the kernel itself waits for that kernel to complete (and its writes to
-// be visible) before touching memory. On by default; PTOC_PDL=0 turns it off
-// (an A/B switch for measurements).
+// be visible) before touching memory. On by default; the documented switch
+// PTOC_PDL=0 turns it off.
 bool programmatic_launch();
 
 // Launchers (one translation unit per element type for the reductions).
