@@ -103,11 +103,33 @@ class Workload:
         inputs of in-place workloads)."""
 
 
+# The library's choice between its two reduction forms (mirrors the rule in
+# ptoc_api.cu, for the kernel label of the bench line only): launches of 2 to
+# 8 ranks on 16-byte-aligned data that move at least 1.5 GiB take the staged
+# form unless PTOC_REDUCE_STAGING forces one.
+STAGED_MIN_BYTES = 3 << 29
+
+
+def reduce_form(nbytes, nranks):
+    forced = os.environ.get("PTOC_REDUCE_STAGING")
+    if not 2 <= nranks <= 8:
+        return "regs"
+    if forced in ("bulk", "regs"):
+        return forced
+    return "bulk" if nbytes >= STAGED_MIN_BYTES else "regs"
+
+
+def reduce_kernel_label(nbytes, nranks, what):
+    if reduce_form(nbytes, nranks) == "bulk":
+        return "reduce_staged_kernel<%s> (sources staged in shared memory by bulk copies, one block per tile)" % what
+    return "reduce_kernel<%s> (sources loaded into registers, one block per tile)" % what
+
+
 class TreduceBench(Workload):
     def __init__(self, w, storage):
         self.w, self.storage = w, storage
         self.name = w.name
-        self.kernel = "reduce_kernel<%s> (one block per tile)" % storage
+        self.kernel = reduce_kernel_label(w.algorithmic_bytes(), w.nranks, "%s, %s" % (storage, "/".join(w.ops)))
         self.dtype_compute = "i32" if storage == "i32" else "f32"
 
     def bytes_per_launch(self):
@@ -313,7 +335,7 @@ class TreducePairBench(Workload):
         w = parts[0].w
         assert all(p.w.algorithmic_bytes() == w.algorithmic_bytes() and len(p.w.ops) == 1 for p in parts)
         self.name = "treduce_n8_16384x8192_f32sum_i32max"
-        self.kernel = "reduce_kernel<f32, Sum> and reduce_kernel<i32, Max> (one block per tile)"
+        self.kernel = " and ".join(p.kernel for p in parts)
         self.dtype_compute = "+".join(p.dtype_compute for p in parts)
 
     def bytes_per_launch(self):

@@ -67,6 +67,17 @@
  *                        tiles down in proportion). It trades
  *                        scheduling granularity against per-tile overhead;
  *                        any other value means the default.
+ *   PTOC_REDUCE_STAGING=bulk|regs
+ *                        how the reductions (ptoc_treduce, ptoc_reduce_scatter,
+ *                        ptoc_allreduce) over 2 to 8 ranks with 16-byte-aligned
+ *                        data load their sources: "bulk" stages each rank's
+ *                        4 KiB tile segment in shared memory with the
+ *                        bulk-copy (TMA) engine, "regs" loads it into
+ *                        registers. Unset (or any other value): "bulk" for
+ *                        launches that move at least 1.5 GiB (N reads plus
+ *                        the writes), "regs" below, the faster form at each
+ *                        size on GB300. Same tiles, grid, arithmetic and
+ *                        stores either way, so results are identical.
  */
 #ifndef PTOC_H
 #define PTOC_H
@@ -351,6 +362,19 @@ ptoc_status ptoc_credit_barrier_host(const ptoc_group* signals, int32_t rank, in
  * (the host-side reset the page prescribes after an aborted call).
  */
 ptoc_status ptoc_signal_reset(const ptoc_group* signals, cudaStream_t stream);
+
+/*
+ * ptoc_wait_faults - failure detection for the waits inside the library's
+ * kernels (no counterpart in the pages). Every wait of the staged reduction
+ * on a bulk copy is bounded (2 s); a block whose wait gives up stores nothing
+ * more and counts one fault on its device. *count receives the faults counted
+ * on the current device since the previous call, and the count restarts at
+ * zero. 0 means every staged tile of every earlier call was stored. The
+ * read is a synchronous copy on the legacy default stream: call it when the
+ * device is idle (after cudaDeviceSynchronize) to include every earlier call.
+ * The credit barrier reports its own waits through its status array.
+ */
+ptoc_status ptoc_wait_faults(uint32_t* count);
 
 /* A static, human-readable name for a status code. */
 const char* ptoc_status_string(ptoc_status status);

@@ -27,13 +27,19 @@ def test_header_declares_the_abi():
                                     "ptoc_all_to_all_v_noalloc", "ptoc_allgather", "ptoc_allreduce", "ptoc_broadcast",
                                     "ptoc_credit_barrier", "ptoc_credit_barrier_host", "ptoc_reduce_scatter",
                                     "ptoc_signal_reset",
-                                    "ptoc_status_string", "ptoc_treduce"]
+                                    "ptoc_status_string", "ptoc_treduce", "ptoc_wait_faults"]
 
 
 def test_library_exports_every_declared_symbol():
     lib = ctypes.CDLL(P.LIB_PATH)
     for name in declared_functions():
         assert hasattr(lib, name), name
+
+
+def test_wait_faults_refuses_a_null_output():
+    lib = ctypes.CDLL(P.LIB_PATH)
+    lib.ptoc_wait_faults.argtypes = [ctypes.c_void_p]
+    assert lib.ptoc_wait_faults(None) == P.ERR_INVALID_ARG
 
 
 def test_status_strings():

@@ -24,6 +24,7 @@ Entry points carry the C names:
                         stream=None)
     ptoc_credit_barrier_host(signals, rank, generations, timeout_ns, status)
     ptoc_signal_reset(signals, stream=None)
+    ptoc_wait_faults()   (returns the count)
 
 Buffers are torch tensors or raw device addresses (ints). ``stream=None``
 means torch's current stream. A non-OK status raises :class:`PtocError`
@@ -87,6 +88,8 @@ for _f in ("ptoc_treduce", "ptoc_reduce_scatter", "ptoc_allgather", "ptoc_all_to
            "ptoc_allreduce", "ptoc_broadcast", "ptoc_all_to_all", "ptoc_all_to_all_v_combine",
            "ptoc_credit_barrier", "ptoc_credit_barrier_host", "ptoc_signal_reset"):
     getattr(_lib, _f).restype = ctypes.c_int
+_lib.ptoc_wait_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+_lib.ptoc_wait_faults.restype = ctypes.c_int
 _lib.ptoc_status_string.argtypes = [ctypes.c_int]
 _lib.ptoc_status_string.restype = ctypes.c_char_p
 
@@ -234,6 +237,15 @@ def ptoc_signal_reset(signals, stream=None, check=True):
     g, keep = _group(signals)
     st = _lib.ptoc_signal_reset(ctypes.byref(g), _stream(stream))
     return _done(st, "ptoc_signal_reset", check)
+
+
+def ptoc_wait_faults(check=True):
+    """The count of staged-reduction waits that gave up on the current device
+    since the previous call (the count then restarts at zero)."""
+    n = ctypes.c_uint32(0)
+    st = _lib.ptoc_wait_faults(ctypes.byref(n))
+    _done(st, "ptoc_wait_faults", check)
+    return int(n.value) if st == OK else st
 
 
 # ---- shape-inferring conveniences over torch tensors ------------------------

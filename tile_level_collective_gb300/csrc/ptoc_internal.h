@@ -36,6 +36,7 @@ struct ReduceParams {
     int32_t tail;                 // elements after the last full vector of a row
     int32_t nranks;
     int32_t dst_mode;             // DstMode
+    int32_t staged;               // 1: the staged form where it applies (host-side choice)
 };
 
 // allgather / broadcast: same box description; win[r] is rank r's window.
@@ -95,6 +96,13 @@ cudaError_t launch_credit_barrier(const BarrierParams& p, cudaStream_t s);
 // PTOC_PDL=0 turns it off.
 bool programmatic_launch();
 
+// Whether a reduction that moves `bytes` per launch takes the staged form
+// (sources copied into shared memory by the bulk-copy engine) where it
+// applies (2 to kGroup ranks, 16-byte vectors) rather than the register form:
+// by size, unless the documented switch PTOC_REDUCE_STAGING (bulk | regs)
+// forces one.
+bool staged_reduction(int64_t bytes);
+
 // Launchers (one translation unit per element type for the reductions).
 // `vb` is the vector width in bytes (16, 8 or 4; 2 for 16-bit data that is
 // only 2-byte aligned). They return the launch status; they never allocate.
@@ -102,6 +110,12 @@ cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int vb, dim3 grid, 
 cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
+// Per element type: read the count of staged tiles whose wait on a copy gave
+// up (in that translation unit's device memory) and reset it to zero.
+cudaError_t take_stage_faults_f32(uint32_t* count);
+cudaError_t take_stage_faults_i32(uint32_t* count);
+cudaError_t take_stage_faults_f16(uint32_t* count);
+cudaError_t take_stage_faults_bf16(uint32_t* count);
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_a2av(const A2avParams& p, int vb, int unroll, dim3 grid, cudaStream_t s);
 // Claiming launches (counts on the device): blocks per SM, and the launch

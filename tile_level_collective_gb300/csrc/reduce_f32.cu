@@ -9,4 +9,9 @@ cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int vb, dim3 grid, 
     return launch_reduce_t<float>(p, op, vb, grid, s);
 }
 
+cudaError_t take_stage_faults_f32(uint32_t* count)
+{
+    return take_stage_faults(count);
+}
+
 }  // namespace ptoc
