@@ -540,6 +540,17 @@ class RsAgBench(Workload):
         oracle.allgather(wins, rows, c["cols"], c["ld"], oracle.F16)
         return _windows_parity(self.dev, wins, rows, c["rows"])
 
+    def oracle_parity_all(self, threads=None):
+        """Every element of every resident window against the oracle's
+        reduce_scatter then allgather over the whole windows (their own chunk
+        bounds), bit for bit."""
+        import oracle
+        c = self.cfg
+        wins = [h.copy() for h in self.host]                 # the oracle works in place
+        oracle.reduce_scatter(wins, c["rows"], c["cols"], c["ld"], oracle.SUM, oracle.F16)
+        oracle.allgather(wins, c["rows"], c["cols"], c["ld"], oracle.F16)
+        return _windows_parity(self.dev, wins, c["rows"], c["rows"])
+
     def oracle_rows_per_second(self):
         nb, dt, _ = self.oracle_sample(64)
         return 64.0 / max(dt, 1e-9)
@@ -796,6 +807,33 @@ class WindowOpBench(Workload):
         else:
             oracle.broadcast(wins, 0, rows, c["cols"], c["ld"], oracle.F16)
         return _windows_parity(self.dev, wins, rows, c["rows"])
+
+    def oracle_parity_all(self, threads=None):
+        """Every element of every resident window against the oracle over the
+        whole windows, bit for bit. Both operations act row by row, so the
+        oracle runs on contiguous row slices of the windows, one host thread
+        each."""
+        import oracle
+        from concurrent.futures import ThreadPoolExecutor
+        c = self.cfg
+        rows = c["rows"]
+        threads = threads or os.cpu_count() or 1
+        wins = [h.copy() for h in self.host]                 # the oracle works in place
+        bounds = [rows * t // threads for t in range(threads + 1)]
+
+        def part(t):
+            a, b = bounds[t], bounds[t + 1]
+            if b <= a:
+                return
+            sl = [w[a:b] for w in wins]
+            if self.op == "allreduce":
+                oracle.allreduce(sl, b - a, c["cols"], c["ld"], oracle.SUM, oracle.F16)
+            else:
+                oracle.broadcast(sl, 0, b - a, c["cols"], c["ld"], oracle.F16)
+
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(part, range(threads)))
+        return _windows_parity(self.dev, wins, rows, rows)
 
     def oracle_rows_per_second(self):
         nb, dt, _ = self.oracle_sample(64)

@@ -139,7 +139,11 @@ def test_window_samples_leave_the_inputs_alone(name):
     wl.dev = [torch.from_numpy(w.view(np.int16).copy()) for w in want]      # stand-ins for the resident run
     assert wl.oracle_parity(12)["result"] == "bit-exact"
     assert wl.oracle_parity(5)["result"] == "bit-exact"
+    # the full-size leg: every row of every window, row slices on threads
+    assert wl.oracle_parity_all(threads=5)["result"] == "bit-exact"
     assert all(np.array_equal(a, b) for a, b in zip(before, wl.host))
+    wl.dev[2][11, 39] ^= 1
+    assert wl.oracle_parity_all(threads=3)["result"] == "MISMATCH in windows 2"
 
 
 @pytest.mark.parametrize("name", ["a2av", "a2av_sparse", "all_to_all", "combine"])
