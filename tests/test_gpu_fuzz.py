@@ -1,10 +1,11 @@
 """Seeded random configurations of every data entry point against the oracle:
-rank counts from 1 to 20 (both reduction forms and the rank groups beyond
+rank counts from 1 to 20 (every rank form and the rank groups beyond
 them), ragged shapes, pitches wider than the rows, rows of several tiles, valid boxes from empty to
 full, every root, buffers placed off the 16-byte grid (so every vector width
 runs), Max / Min / Sum / Prod, and exchange counts that are negative, zero,
 within and beyond capacity. Every buffer carries guard bands; results must
-match bit for bit (any NaN equal to any NaN for computed floating results)."""
+match bit for bit (any NaN equal to any NaN for computed floating results).
+The staged reduction form is forced on random cases too."""
 import numpy as np
 import pytest
 import torch
@@ -204,3 +205,55 @@ def test_fuzz_all_to_all_and_combine(seed):
         for s in range(n):
             assert nan_equal(d_out[s].host(), outs[s], dtype), "combine %s atomic %d output %d" % (dtype, atomic, s)
             assert d_out[s].guards_intact() and d_rc[s].guards_intact()
+
+
+def aligned_pitch(rng, cols, eb):
+    """A pitch of at least `cols` elements that is a multiple of 16 bytes (the
+    staged form's condition), or any pitch one time in four."""
+    ld = cols + int(rng.integers(0, 9))
+    if rng.random() < 0.75:
+        q = 16 // eb
+        ld = (ld + q - 1) // q * q
+    return ld
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_fuzz_staged_form(seed, monkeypatch):
+    """The staged reduction form, forced (its size rule keeps cases this small
+    in registers), on random TREDUCE cases over 1 to 10 ranks, mostly
+    16-byte-aligned (2 to 8 ranks on aligned buffers and pitch take the staged
+    form, the rest the register form), rows of one or several tiles, and on
+    the window reductions; no staged wait gives up."""
+    monkeypatch.setenv("PTOC_REDUCE_STAGING", "bulk")
+    P.ptoc_wait_faults()
+    rng = np.random.default_rng(5000 + seed)
+    for i in range(60):
+        dtype = DTYPES[int(rng.integers(4))]
+        eb = ELEM_BYTES[dtype]
+        n = int(rng.integers(1, 11))
+        rows, cols, _ = wide_shape(rng) if i % 3 == 0 else shape(rng)
+        ld = aligned_pitch(rng, cols, eb)
+        off = 0 if rng.random() < 0.8 else offset(rng, eb)
+        if i % 4 != 3:
+            op = ["sum", "max", "min"][int(rng.integers(3))]
+            vr, vc = int(rng.integers(0, rows + 1)), int(rng.integers(0, cols + 1))
+            run_case(dtype, op, n, rows, cols, ld, vr, vc, root=int(rng.integers(n)), offset=off,
+                     inplace=bool(rng.random() < 0.2), seed=int(rng.integers(1 << 30)), specials=True)
+            continue
+        op = ["sum", "max", "min", "prod"][int(rng.integers(4))]
+        host = windows_host(dtype, n, rows, cols, ld, seed=int(rng.integers(1 << 30)))
+        dev = [DevBuf(h, off) for h in host]
+        ptrs = [d.ptr for d in dev]
+        if rng.random() < 0.5:
+            P.ptoc_reduce_scatter(ptrs, rows, cols, ld, OP4[op][0], PCODE[dtype])
+            assert oracle.reduce_scatter(host, rows, cols, ld, OP4[op][1], ORC_DT[dtype]) == 0
+        else:
+            P.ptoc_allreduce(ptrs, rows, cols, ld, OP4[op][0], PCODE[dtype])
+            assert oracle.allreduce(host, rows, cols, ld, OP4[op][1], ORC_DT[dtype]) == 0
+        torch.cuda.synchronize()
+        for r in range(n):
+            assert nan_equal(dev[r].host(), host[r], dtype), "%s %s n=%d %dx%d ld %d window %d" % (
+                op, dtype, n, rows, cols, ld, r)
+            assert dev[r].guards_intact()
+    torch.cuda.synchronize()
+    assert P.ptoc_wait_faults() == 0
