@@ -1,8 +1,9 @@
 """Library calls captured in a CUDA graph and replayed: the parameters
 (pointers, sizes) are baked into the graph, every replay recomputes from the
-current buffer contents, and results stay bit-exact against the oracle. The
-first call of each kernel on a device (which queries occupancy and opts the
-kernel into its shared memory) is made before capture."""
+current buffer contents, and results stay bit-exact against the oracle, with
+the reductions in either form. The first call of each kernel on a device
+(which queries occupancy and opts the kernel into its shared memory) is made
+before capture."""
 import numpy as np
 import pytest
 import torch
@@ -15,7 +16,10 @@ from gpu_util import to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 
-def test_graph_replay_of_a_collective_pipeline():
+@pytest.mark.parametrize("form", ["regs", "bulk"])
+def test_graph_replay_of_a_collective_pipeline(form, monkeypatch):
+    """Both reduction forms (PTOC_REDUCE_STAGING), captured and replayed."""
+    monkeypatch.setenv("PTOC_REDUCE_STAGING", form)
     n, rows, cols, ld = 4, 96, 1000, 1024
     rng = np.random.default_rng(0)
     hosts = [synth.f32_to_bf16_bits(rng.standard_normal((rows, ld)).astype(np.float32)).reshape(rows, ld)

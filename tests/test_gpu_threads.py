@@ -46,7 +46,12 @@ def worker(tid, errors):
         errors.append("thread %d: %r" % (tid, e))
 
 
-def test_concurrent_host_threads():
+@pytest.mark.parametrize("form", ["regs", "bulk"])
+def test_concurrent_host_threads(form, monkeypatch):
+    """With PTOC_REDUCE_STAGING=bulk the 16-byte-aligned cases (threads 0 and
+    4) run the staged form, concurrently with the others' register form."""
+    monkeypatch.setenv("PTOC_REDUCE_STAGING", form)
+    P.ptoc_wait_faults()
     errors = []
     threads = [threading.Thread(target=worker, args=(t, errors)) for t in range(8)]
     for t in threads:
@@ -54,3 +59,5 @@ def test_concurrent_host_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+    torch.cuda.synchronize()
+    assert P.ptoc_wait_faults() == 0
