@@ -67,17 +67,24 @@
  *                        tiles down in proportion). It trades
  *                        scheduling granularity against per-tile overhead;
  *                        any other value means the default.
- *   PTOC_REDUCE_STAGING=bulk|regs
+ *   PTOC_REDUCE_STAGING=bulk|regs|tma
  *                        how the reductions (ptoc_treduce, ptoc_reduce_scatter,
  *                        ptoc_allreduce) over 2 to 8 ranks with 16-byte-aligned
  *                        data load their sources: "bulk" stages each rank's
  *                        4 KiB tile segment in shared memory with the
  *                        bulk-copy (TMA) engine, "regs" loads it into
- *                        registers. Unset (or any other value): "bulk" for
- *                        launches that move at least 1.5 GiB (N reads plus
- *                        the writes), "regs" below, the faster form at each
- *                        size on GB300. Same tiles, grid, arithmetic and
- *                        stores either way, so results are identical.
+ *                        registers (same tiles, grid, arithmetic and stores).
+ *                        "tma" runs ptoc_treduce through tensor maps over the
+ *                        valid box: 2-D boxes of every rank loaded into shared
+ *                        memory, the result box stored back by the tensor
+ *                        engine, clipped to the valid box; it applies when
+ *                        every base pointer, the pitch and a valid row are
+ *                        multiples of 16 bytes (else, and for the window
+ *                        reductions, the register form runs). Unset (or any
+ *                        other value): "bulk" for launches that move at
+ *                        least 1.5 GiB (N reads plus the writes), "regs"
+ *                        below, the faster form at each size on GB300.
+ *                        Results are identical in every form.
  */
 #ifndef PTOC_H
 #define PTOC_H

@@ -217,14 +217,16 @@ def aligned_pitch(rng, cols, eb):
     return ld
 
 
+@pytest.mark.parametrize("form", ["bulk", "tma"])
 @pytest.mark.parametrize("seed", range(4))
-def test_fuzz_staged_form(seed, monkeypatch):
+def test_fuzz_staged_form(seed, form, monkeypatch):
     """The staged reduction form, forced (its size rule keeps cases this small
     in registers), on random TREDUCE cases over 1 to 10 ranks, mostly
     16-byte-aligned (2 to 8 ranks on aligned buffers and pitch take the staged
     form, the rest the register form), rows of one or several tiles, and on
-    the window reductions; no staged wait gives up."""
-    monkeypatch.setenv("PTOC_REDUCE_STAGING", "bulk")
+    the window reductions; no staged wait gives up. The same with the tensor
+    form of TREDUCE."""
+    monkeypatch.setenv("PTOC_REDUCE_STAGING", form)
     P.ptoc_wait_faults()
     rng = np.random.default_rng(5000 + seed)
     for i in range(60):

@@ -16,7 +16,7 @@ from gpu_util import to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("form", ["regs", "bulk"])
+@pytest.mark.parametrize("form", ["regs", "bulk", "tma"])
 def test_graph_replay_of_a_collective_pipeline(form, monkeypatch):
     """Both reduction forms (PTOC_REDUCE_STAGING), captured and replayed."""
     monkeypatch.setenv("PTOC_REDUCE_STAGING", form)

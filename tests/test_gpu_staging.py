@@ -1,10 +1,13 @@
-"""Both source-loading forms of the reductions (PTOC_REDUCE_STAGING=regs: the
-sources go into registers; =bulk: the bulk-copy engine stages each rank's tile
-segment in shared memory) against the oracle, bit for bit: the odd small
-shapes of TREDUCE, in place, reduce_scatter + allgather and allreduce, then
-the TREDUCE workloads and the 8-window reduce_scatter at full size. Both forms
-share tiles, arithmetic and stores, so they must agree everywhere; after each
-test no staged wait has given up (ptoc_wait_faults)."""
+"""Every source-loading form of the reductions against the oracle, bit for bit
+(PTOC_REDUCE_STAGING=regs: the sources go into registers; =bulk: the
+bulk-copy engine stages each rank's tile segment in shared memory; =tma:
+TREDUCE through tensor maps over the valid box, 2-D boxes loaded into shared
+memory and the result box stored back clipped to the valid box; the window
+reductions run the register form under it): the odd small shapes of TREDUCE,
+in place, reduce_scatter + allgather and allreduce, then the TREDUCE workloads
+and the 8-window reduce_scatter at full size. The forms share the fold
+arithmetic, so they must agree everywhere; after each test no staged wait has
+given up (ptoc_wait_faults)."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +22,7 @@ from test_gpu_treduce import PCODE, SMALL, run_case
 
 pytestmark = pytest.mark.gpu
 
-FORMS = ["regs", "bulk"]
+FORMS = ["regs", "bulk", "tma"]
 
 
 @pytest.fixture(params=FORMS)

@@ -46,7 +46,7 @@ def worker(tid, errors):
         errors.append("thread %d: %r" % (tid, e))
 
 
-@pytest.mark.parametrize("form", ["regs", "bulk"])
+@pytest.mark.parametrize("form", ["regs", "bulk", "tma"])
 def test_concurrent_host_threads(form, monkeypatch):
     """With PTOC_REDUCE_STAGING=bulk the 16-byte-aligned cases (threads 0 and
     4) run the staged form, concurrently with the others' register form."""

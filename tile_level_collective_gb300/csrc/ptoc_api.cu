@@ -45,8 +45,16 @@ bool staged_reduction(int64_t bytes)
 {
     const char* e = getenv("PTOC_REDUCE_STAGING");
     if (e && strcmp(e, "bulk") == 0) return true;
-    if (e && strcmp(e, "regs") == 0) return false;
+    if (e && (strcmp(e, "regs") == 0 || strcmp(e, "tma") == 0)) return false;
     return bytes >= kStagedMinBytes;
+}
+
+// Whether TREDUCE takes the tensor form (PTOC_REDUCE_STAGING=tma) where it
+// applies.
+bool tensor_form_selected()
+{
+    const char* e = getenv("PTOC_REDUCE_STAGING");
+    return e && strcmp(e, "tma") == 0;
 }
 
 namespace {
@@ -212,6 +220,79 @@ dim3 grid_for(int64_t ntiles)
     // large boxes fall back to a grid-stride loop inside the kernel.
     const int64_t cap = (int64_t)1 << 30;
     return dim3((unsigned)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap));
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point
+// (the library links no driver library); null if the driver lacks it.
+using TensorMapEncoder = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+TensorMapEncoder tensor_map_encoder()
+{
+    static std::once_flag once;
+    static TensorMapEncoder fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = (TensorMapEncoder)f;
+    });
+    return fn;
+}
+
+// A tensor map over the valid box of a slice: {valid_cols, valid_rows}
+// elements, rows ld * eb bytes apart, boxes of kTmaBoxCols x (4 KiB / row
+// bytes) elements, zero fill outside. False if the driver refuses it.
+bool encode_valid_box(CUtensorMap* m, const void* base, int eb, int64_t valid_rows, int64_t valid_cols, int64_t ld)
+{
+    const TensorMapEncoder enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)valid_cols, (cuuint64_t)valid_rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * eb)};
+    const cuuint32_t box[2] = {(cuuint32_t)kTmaBoxCols, (cuuint32_t)(kBlock * 16 / (kTmaBoxCols * eb))};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return enc(m, eb == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+               const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// TREDUCE in the tensor form, if it applies: 2 to kGroup ranks, every base
+// pointer, the row pitch and a row of the valid box a multiple of 16 bytes
+// (a tensor store clips a row at 16-byte granularity, so a valid row that
+// ends inside a 16-byte unit would have its padding overwritten), extents
+// that fit a tensor map. Returns false (nothing launched) when it does not
+// apply; otherwise the launch status in *e.
+bool launch_tensor_form(int dtype, const void* const* src, void* dst, int n, int op, int64_t valid_rows,
+                        int64_t valid_cols, int64_t ld, int eb, cudaStream_t stream, cudaError_t* e)
+{
+    if (n < 2 || n > kGroup) return false;
+    if (((uintptr_t)dst & 15u) || ((ld * eb) & 15) || ((valid_cols * eb) & 15)) return false;
+    for (int r = 0; r < n; ++r)
+        if ((uintptr_t)src[r] & 15u) return false;
+    if (valid_cols > ((int64_t)1 << 32) || valid_rows > ((int64_t)1 << 32) || ld * eb >= ((int64_t)1 << 40))
+        return false;
+    TmaReduceParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < n; ++r)
+        if (!encode_valid_box(&p.src[r], src[r], eb, valid_rows, valid_cols, ld)) return false;
+    if (!encode_valid_box(&p.dst, dst, eb, valid_rows, valid_cols, ld)) return false;
+    const int64_t box_rows = kBlock * 16 / (kTmaBoxCols * eb);
+    const int64_t tiles_x = (valid_cols + kTmaBoxCols - 1) / kTmaBoxCols;
+    const int64_t tiles_y = (valid_rows + box_rows - 1) / box_rows;
+    if (tiles_x > INT32_MAX) return false;
+    p.tiles_x = (int32_t)tiles_x;
+    p.ntiles = tiles_x * tiles_y;
+    p.nranks = n;
+    switch (dtype) {
+    case PTOC_F32: *e = launch_tma_reduce_f32(p, op, stream); break;
+    case PTOC_I32: *e = launch_tma_reduce_i32(p, op, stream); break;
+    case PTOC_F16: *e = launch_tma_reduce_f16(p, op, stream); break;
+    default: *e = launch_tma_reduce_bf16(p, op, stream); break;
+    }
+    return true;
 }
 
 cudaError_t launch_reduce_regs(int dtype, const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s)
@@ -429,6 +510,12 @@ extern "C" ptoc_status ptoc_treduce(const ptoc_group* group, void* dst, int64_t 
     // One rank: a bit copy (TREDUCE article §4.3). Max with a single operand
     // is exactly that, NaN payloads included.
     const int eff_op = (n == 1) ? PTOC_MAX : (int)op;
+
+    if (tensor_form_selected()) {
+        cudaError_t e = cudaSuccess;
+        if (launch_tensor_form(dtype, p.src, dst, n, eff_op, valid_rows, valid_cols, ld, eb, stream, &e))
+            return e == cudaSuccess ? PTOC_OK : PTOC_ERR_CUDA;
+    }
 
     // Contiguous valid box (full rows, or a single row): one flat row.
     const bool flat = (valid_cols == ld) || (valid_rows == 1);

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>              // CUtensorMap (a type only: the library links no driver library)
 #include <cuda_runtime_api.h>
 
 #include "ptoc.h"
@@ -37,6 +38,26 @@ struct ReduceParams {
     int32_t nranks;
     int32_t dst_mode;             // DstMode
     int32_t staged;               // 1: the staged form where it applies (host-side choice)
+};
+
+// TREDUCE through tensor maps (the tensor form): src[r] describes source r
+// (reduction order, root first) and dst the destination, each over the valid
+// box only: globalDim = {valid_cols, valid_rows}, row stride ld * element
+// bytes, box = kTmaBoxCols elements x box_rows rows (4 KiB). Loads of a box
+// that reaches past the valid box fill the outside with zeros; stores clip
+// at it, so padding is never written. Tile w is the box at column
+// (w % tiles_x) * kTmaBoxCols, row (w / tiles_x) * box_rows. Stores clip a
+// row at 16-byte granularity, so the form needs valid rows of a multiple of
+// 16 bytes (the host checks it). Passed by value
+// as a __grid_constant__ parameter (tensor maps must live in parameter,
+// constant or global memory).
+constexpr int kTmaBoxCols = 256;
+struct TmaReduceParams {
+    CUtensorMap src[kGroup];
+    CUtensorMap dst;
+    int64_t ntiles;
+    int32_t tiles_x;
+    int32_t nranks;
 };
 
 // allgather / broadcast: same box description; win[r] is rank r's window.
@@ -110,6 +131,12 @@ cudaError_t launch_reduce_f32(const ReduceParams& p, int op, int vb, dim3 grid, 
 cudaError_t launch_reduce_i32(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_bf16(const ReduceParams& p, int op, int vb, dim3 grid, cudaStream_t s);
+// The tensor form of TREDUCE, per element type (4 or 2 bytes: the copies
+// move bits, the fold is the type's).
+cudaError_t launch_tma_reduce_f32(const TmaReduceParams& p, int op, cudaStream_t s);
+cudaError_t launch_tma_reduce_i32(const TmaReduceParams& p, int op, cudaStream_t s);
+cudaError_t launch_tma_reduce_f16(const TmaReduceParams& p, int op, cudaStream_t s);
+cudaError_t launch_tma_reduce_bf16(const TmaReduceParams& p, int op, cudaStream_t s);
 // Per element type: read the count of staged tiles whose wait on a copy gave
 // up (in that translation unit's device memory) and reset it to zero.
 cudaError_t take_stage_faults_f32(uint32_t* count);

@@ -9,6 +9,11 @@ cudaError_t launch_reduce_f16(const ReduceParams& p, int op, int vb, dim3 grid, 
     return launch_reduce_t<__half>(p, op, vb, grid, s);
 }
 
+cudaError_t launch_tma_reduce_f16(const TmaReduceParams& p, int op, cudaStream_t s)
+{
+    return launch_tma_reduce_t<__half>(p, op, s);
+}
+
 cudaError_t take_stage_faults_f16(uint32_t* count)
 {
     return take_stage_faults(count);

@@ -707,6 +707,125 @@ __global__ void __launch_bounds__(kBlock) reduce_staged_kernel(const __grid_cons
     }
 }
 
+// ---- the tensor form (TREDUCE) -----------------------------------------------
+
+// One box of 256 threads x 16 bytes = 4 KiB per rank: kTmaBoxCols elements
+// wide, this many rows high (4 for 4-byte elements, 8 for 2-byte ones).
+template <class T>
+constexpr int kTmaBoxRows = kBlock * 16 / (kTmaBoxCols * (int)sizeof(T));
+
+// Arm the mbarrier at `bar` for one 4 KiB box and load the box at (x, y) of
+// the tensor map `map` (a kernel-parameter address) into shared `dst`.
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kBlock * 16) : "memory");
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+                 : "memory");
+}
+
+// Store the 4 KiB box in shared `src` at (x, y) of `map`, clipped to the
+// map's extent; returns once shared memory has been read.
+__device__ __forceinline__ void tma_store_box(const CUtensorMap* map, int x, int y, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// TREDUCE over 2 to kGroup ranks through tensor maps. Tile w is one box of
+// the valid box: threads 0..n-1 each load their rank's box into shared
+// memory (rank r at r * kBlock vectors), completing on that rank's mbarrier;
+// every thread folds its 16 bytes of the box over the ranks in order as the
+// boxes land (parts of a box outside the valid box were filled with zeros
+// and fold to values that are never stored), writes the result over rank 0's
+// box, and thread 0 stores the box, which the map clips to the valid box.
+// Waits are bounded as in the staged form; a block that gives up counts a
+// fault and returns without storing.
+template <class T, int OP>
+__global__ void __launch_bounds__(kBlock) reduce_tma2d_kernel(const __grid_constant__ TmaReduceParams p)
+{
+    extern __shared__ __align__(128) Words<4> stage[];
+    __shared__ __align__(8) uint64_t bars[kGroup];
+    constexpr int kRows = kTmaBoxRows<T>;
+    const int n = p.nranks;
+    const int tid = threadIdx.x;
+    // the boxes need 128-byte-aligned shared memory: refuse rather than copy
+    if (smem_u32(stage) & 127u) {
+        if (tid == 0) atomicAdd(&g_stage_faults, 1u);
+        return;
+    }
+    auto issue = [&](int64_t w) {
+        const int x = (int)(w % p.tiles_x) * kTmaBoxCols;
+        const int y = (int)(w / p.tiles_x) * kRows;
+        tma_load_box(smem_u32(stage + tid * kBlock), &p.src[tid], x, y, smem_u32(&bars[tid]));
+    };
+    if (tid < n) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[tid])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_enter();
+    if (blockIdx.x < p.ntiles && tid < n) issue(blockIdx.x);
+    __syncthreads();              // every mbarrier is initialised before anyone waits on it
+    uint32_t parity = 0;
+    bool first = true;
+    for (int64_t w = blockIdx.x; w < p.ntiles; w += gridDim.x) {
+        if (!first && tid < n) {
+            // the stage was last read through the generic proxy (previous tile)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(w);
+        }
+        first = false;
+        const uint64_t deadline = globaltimer_ns() + kStageWaitNs;
+        const uint32_t mine = smem_u32(stage + tid);
+        VecAcc<T, OP, 4> acc;
+        bool ok = stage_wait(smem_u32(&bars[0]), parity, deadline);
+        if (ok) acc.init(stage_load(mine));
+        for (int r = 1; r < n && ok; ++r) {
+            ok = stage_wait(smem_u32(&bars[r]), parity, deadline);
+            if (ok) acc.add(stage_load(mine + (uint32_t)(r * kBlock * 16)));
+        }
+        if (ok) {
+            const Words<4> v = acc.out();
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                         ::"r"(mine), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                         : "memory");
+        }
+        // the result box is complete (and visible to the async proxy) before
+        // thread 0 stores it; a failed wait anywhere skips the store
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) atomicAdd(&g_stage_faults, 1u);
+            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs);
+            __syncthreads();
+            return;
+        }
+        if (tid == 0)
+            tma_store_box(&p.dst, (int)(w % p.tiles_x) * kTmaBoxCols, (int)(w / p.tiles_x) * kRows,
+                          smem_u32(stage));
+        __syncthreads();          // the store has read the stage before it is refilled
+        parity ^= 1u;
+    }
+}
+
+template <class T>
+cudaError_t launch_tma_reduce_t(const TmaReduceParams& p, int op, cudaStream_t s)
+{
+    if (p.nranks < 2 || p.nranks > kGroup || p.ntiles < 1) return cudaErrorInvalidValue;
+    const int64_t cap = (int64_t)1 << 30;
+    const dim3 grid((unsigned)(p.ntiles < cap ? p.ntiles : cap));
+    const size_t smem = (size_t)p.nranks * kBlock * 16;
+    switch (op) {
+    case kSum: return launch_kernel(reduce_tma2d_kernel<T, kSum>, grid, kBlock, smem, s, p);
+    case kMax: return launch_kernel(reduce_tma2d_kernel<T, kMax>, grid, kBlock, smem, s, p);
+    case kMin: return launch_kernel(reduce_tma2d_kernel<T, kMin>, grid, kBlock, smem, s, p);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 // The rank form follows the rank count; kWide runs on vectors of at most 8
 // bytes (the host narrows 16-byte vectors for 9 to 16 ranks).
 template <class T, int OP, int VB>
