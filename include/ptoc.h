@@ -85,6 +85,14 @@
  *                        least 1.5 GiB (N reads plus the writes), "regs"
  *                        below, the faster form at each size on GB300.
  *                        Results are identical in every form.
+ *   PTOC_WAIT_NS=<ns>    the bound on one wait of the staged and tensor forms
+ *                        for a copy to land (1 ns to 60 s; default 2 s). A
+ *                        block whose wait runs out stores nothing more,
+ *                        counts a fault (ptoc_wait_faults), waits (bounded,
+ *                        2 s) for its own copies in flight and returns, so
+ *                        part of that call's result is missing. Copies of
+ *                        valid memory land in microseconds; tiny bounds serve
+ *                        to exercise the detection path.
  */
 #ifndef PTOC_H
 #define PTOC_H
@@ -372,9 +380,9 @@ ptoc_status ptoc_signal_reset(const ptoc_group* signals, cudaStream_t stream);
 
 /*
  * ptoc_wait_faults - failure detection for the waits inside the library's
- * kernels (no counterpart in the pages). Every wait of the staged reduction
- * on a bulk copy is bounded (2 s); a block whose wait gives up stores nothing
- * more and counts one fault on its device. *count receives the faults counted
+ * kernels (no counterpart in the pages). Every wait of the staged and tensor
+ * reduction forms on a copy is bounded (2 s, or PTOC_WAIT_NS); a block whose
+ * wait gives up stores nothing more and counts one fault on its device. *count receives the faults counted
  * on the current device since the previous call, and the count restarts at
  * zero. 0 means every staged tile of every earlier call was stored. The
  * read is a synchronous copy on the legacy default stream: call it when the

@@ -119,3 +119,39 @@ def test_wait_faults_reads_zero_when_idle():
     torch.cuda.synchronize()
     P.ptoc_wait_faults()
     assert P.ptoc_wait_faults() == 0
+
+
+@pytest.mark.parametrize("kind", ["bulk", "tma"])
+def test_waits_that_run_out_are_counted_and_recovered(kind, monkeypatch):
+    """Failure detection without a GPU fault: with a bound of 1 ns on each
+    wait for a copy (PTOC_WAIT_NS), waits run out. The blocks concerned count
+    a fault, store nothing, wait (with the full bound) for their own copies in
+    flight and return; the launch ends, every element of dst is either still
+    the sentinel or the oracle's value, and the next call with the default
+    bound is complete and counts no fault."""
+    monkeypatch.setenv("PTOC_REDUCE_STAGING", kind)
+    n, rows, cols = 8, 2048, 4096            # f32, 16-byte rows: both forms apply
+    rng = np.random.default_rng(77)
+    host = [rng.standard_normal((rows, cols)).astype(np.float32) for _ in range(n)]
+    dev = [to_dev(h) for h in host]
+    want = np.zeros((rows, cols), np.float32)
+    assert oracle_treduce_threaded(host, want, rows, cols, cols, oracle.SUM, oracle.F32) == 0
+    sentinel = np.full((rows, cols), 0xFFD5FFD5, dtype=np.uint32).view(np.float32)
+    torch.cuda.synchronize()
+    P.ptoc_wait_faults()
+    monkeypatch.setenv("PTOC_WAIT_NS", "1")
+    dst = to_dev(sentinel)
+    P.ptoc_treduce(dev, dst, rows, cols, rows, cols, cols, P.SUM, P.F32)
+    torch.cuda.synchronize()
+    faults = P.ptoc_wait_faults()
+    got = bits(to_host(dst, np.float32))
+    untouched = got == 0xFFD5FFD5
+    assert faults > 0 and untouched.any()
+    assert np.array_equal(got[~untouched], bits(want)[~untouched])
+    monkeypatch.delenv("PTOC_WAIT_NS")
+    dst = to_dev(sentinel)
+    P.ptoc_treduce(dev, dst, rows, cols, rows, cols, cols, P.SUM, P.F32)
+    torch.cuda.synchronize()
+    assert P.ptoc_wait_faults() == 0
+    got = to_host(dst, np.float32)
+    assert np.array_equal(bits(got), bits(want)), first_diff(got, want)

@@ -49,6 +49,17 @@ bool staged_reduction(int64_t bytes)
     return bytes >= kStagedMinBytes;
 }
 
+uint64_t copy_wait_ns()
+{
+    const uint64_t dflt = 2000000000ull, most = 60000000000ull;
+    const char* e = getenv("PTOC_WAIT_NS");
+    if (!e || !*e) return dflt;
+    char* end = nullptr;
+    const unsigned long long v = strtoull(e, &end, 10);
+    if (!end || *end || v < 1) return dflt;
+    return v > most ? most : (uint64_t)v;
+}
+
 // Whether TREDUCE takes the tensor form (PTOC_REDUCE_STAGING=tma) where it
 // applies.
 bool tensor_form_selected()
@@ -286,6 +297,7 @@ bool launch_tensor_form(int dtype, const void* const* src, void* dst, int n, int
     p.tiles_x = (int32_t)tiles_x;
     p.ntiles = tiles_x * tiles_y;
     p.nranks = n;
+    p.wait_ns = copy_wait_ns();
     switch (dtype) {
     case PTOC_F32: *e = launch_tma_reduce_f32(p, op, stream); break;
     case PTOC_I32: *e = launch_tma_reduce_i32(p, op, stream); break;
@@ -328,6 +340,7 @@ cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, i
     const int64_t writes = p.dst_mode == kDstAll ? p.nranks : 1;
     const int64_t elems = rows > 0 && cols > 0 ? rows * cols : 0;
     p.staged = staged_reduction((p.nranks + writes) * eb * elems) ? 1 : 0;
+    p.wait_ns = copy_wait_ns();
     return launch_reduce_regs(dtype, p, op, vb, grid_for(p.ntiles + p.tail_blocks), s);
 }
 

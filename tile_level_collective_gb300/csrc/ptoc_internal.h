@@ -38,6 +38,7 @@ struct ReduceParams {
     int32_t nranks;
     int32_t dst_mode;             // DstMode
     int32_t staged;               // 1: the staged form where it applies (host-side choice)
+    uint64_t wait_ns;             // the staged form's bound on one wait for a copy
 };
 
 // TREDUCE through tensor maps (the tensor form): src[r] describes source r
@@ -56,9 +57,14 @@ struct TmaReduceParams {
     CUtensorMap src[kGroup];
     CUtensorMap dst;
     int64_t ntiles;
+    uint64_t wait_ns;             // bound on one wait for a box
     int32_t tiles_x;
     int32_t nranks;
 };
+
+// The bound, in nanoseconds, on one wait of the staged and tensor forms for a
+// copy: 2 s, or the documented switch PTOC_WAIT_NS (1 ns to 60 s).
+uint64_t copy_wait_ns();
 
 // allgather / broadcast: same box description; win[r] is rank r's window.
 // Row i is read from win[owner(i)] (allgather) or from win[root] when

@@ -608,17 +608,38 @@ __device__ __forceinline__ bool stage_ready(uint32_t bar, uint32_t parity)
 
 // Every wait on a copy is bounded: a deadline on %globaltimer behind an
 // iteration cap. A copy of valid memory always completes long before either.
+// The fold's waits take the launch's bound (wait_ns, 2 s unless the caller's
+// process sets PTOC_WAIT_NS); the one wait of a block that gave up, for its
+// own copies still in flight, always takes kStageWaitNs, so that no block
+// leaves while a copy into its shared memory may still land.
 // Tiles whose wait gave up are counted here (one counter per translation
 // unit, zero at load; ptoc_wait_faults reads and clears them).
 static __device__ uint32_t g_stage_faults;
 constexpr uint64_t kStageWaitNs = 2000000000ull;
 constexpr uint32_t kStageWaitPolls = 1u << 26;
 
-__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint64_t deadline)
+// try_wait with a bound on how long the thread may stay suspended in it
+__device__ __forceinline__ bool stage_ready_within(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounds below this are passed to try_wait as its suspend-time limit, and the
+// deadline is then checked after every poll: try_wait may otherwise stay
+// suspended until the copy lands, well past a short bound.
+constexpr uint64_t kHintedWaitNs = 1000000ull;
+
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint64_t deadline, uint64_t bound_ns)
+{
+    const uint32_t hint = bound_ns < kHintedWaitNs ? (uint32_t)bound_ns : 0u;
     for (uint32_t i = 0; i < kStageWaitPolls; ++i) {
-        if (stage_ready(bar, parity)) return true;
-        if ((i & 31) == 31 && globaltimer_ns() > deadline) return false;
+        if (hint ? stage_ready_within(bar, parity, hint) : stage_ready(bar, parity)) return true;
+        if ((hint || (i & 31) == 31) && globaltimer_ns() > deadline) return false;
     }
     return false;
 }
@@ -685,13 +706,13 @@ __global__ void __launch_bounds__(kBlock) reduce_staged_kernel(const __grid_cons
         issued = false;
         bool ok = true;
         if (tid < nv) {
-            const uint64_t deadline = globaltimer_ns() + kStageWaitNs;
+            const uint64_t deadline = globaltimer_ns() + p.wait_ns;
             const uint32_t mine = smem_u32(stage + tid);
             VecAcc<T, OP, 4> acc;
-            ok = stage_wait(smem_u32(&bars[0]), parity, deadline);
+            ok = stage_wait(smem_u32(&bars[0]), parity, deadline, p.wait_ns);
             if (ok) acc.init(stage_load(mine));
             for (int r = 1; r < n && ok; ++r) {
-                ok = stage_wait(smem_u32(&bars[r]), parity, deadline);
+                ok = stage_wait(smem_u32(&bars[r]), parity, deadline, p.wait_ns);
                 if (ok) acc.add(stage_load(mine + (uint32_t)(r * kBlock * 16)));
             }
             if (ok) store_result<4>(p, row, off0 + (int64_t)tid * 16, acc.out());
@@ -699,7 +720,7 @@ __global__ void __launch_bounds__(kBlock) reduce_staged_kernel(const __grid_cons
         // every thread is done with the stage before it is refilled
         if (!__syncthreads_and(ok)) {
             if (tid == 0) atomicAdd(&g_stage_faults, 1u);
-            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs);
+            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs, kStageWaitNs);
             __syncthreads();
             return;
         }
@@ -779,13 +800,13 @@ __global__ void __launch_bounds__(kBlock) reduce_tma2d_kernel(const __grid_const
             issue(w);
         }
         first = false;
-        const uint64_t deadline = globaltimer_ns() + kStageWaitNs;
+        const uint64_t deadline = globaltimer_ns() + p.wait_ns;
         const uint32_t mine = smem_u32(stage + tid);
         VecAcc<T, OP, 4> acc;
-        bool ok = stage_wait(smem_u32(&bars[0]), parity, deadline);
+        bool ok = stage_wait(smem_u32(&bars[0]), parity, deadline, p.wait_ns);
         if (ok) acc.init(stage_load(mine));
         for (int r = 1; r < n && ok; ++r) {
-            ok = stage_wait(smem_u32(&bars[r]), parity, deadline);
+            ok = stage_wait(smem_u32(&bars[r]), parity, deadline, p.wait_ns);
             if (ok) acc.add(stage_load(mine + (uint32_t)(r * kBlock * 16)));
         }
         if (ok) {
@@ -799,7 +820,7 @@ __global__ void __launch_bounds__(kBlock) reduce_tma2d_kernel(const __grid_const
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (!__syncthreads_and(ok)) {
             if (tid == 0) atomicAdd(&g_stage_faults, 1u);
-            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs);
+            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs, kStageWaitNs);
             __syncthreads();
             return;
         }
