@@ -47,9 +47,14 @@ def test_small_shapes(form, dtype, op):
 @pytest.mark.parametrize("op", ["sum", "max", "min"])
 def test_in_place_and_multi_tile_rows(form, dtype, op):
     run_case(dtype, op, 4, 12, 70, 72, 11, 66, root=2, inplace=True, seed=3)
+    # in place with valid rows of a multiple of 16 bytes (the tensor form applies)
+    run_case(dtype, op, 4, 12, 64, 72, 11, 64, root=1, inplace=True, seed=4)
     # rows of several tiles with a partial last tile, every rank count of one group
     for n in range(2, 9):
         run_case(dtype, op, n, 3, 3000, 3008, 3, 2999, root=n - 1, seed=40 + n)
+        # the same with valid rows of a multiple of 16 bytes: several boxes per
+        # row and a ragged last box for the tensor form
+        run_case(dtype, op, n, 9, 3000, 3008, 7, 2992, root=0, seed=50 + n)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "i32"])
