@@ -71,8 +71,8 @@ class L2Flush:
 # configuration in ptoc_api.cu calls for a new capture too).
 _CSRC = "tile_level_collective_gb300/csrc/"
 _COMMON = [_CSRC + "ptoc_internal.h", _CSRC + "reduce_impl.cuh"]
-REDUCE_SOURCES = _COMMON + [_CSRC + f for f in ("reduce_f32.cu", "reduce_f16.cu", "reduce_bf16.cu",
-                                                "reduce_i32.cu")]
+REDUCE_SOURCES = _COMMON + [_CSRC + f for f in ("reduce_forms.cuh", "reduce_f32.cu", "reduce_f16.cu",
+                                                "reduce_bf16.cu", "reduce_i32.cu")]
 MOVE_SOURCES = _COMMON + [_CSRC + "movement.cu"]
 
 

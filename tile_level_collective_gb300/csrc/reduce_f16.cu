@@ -1,6 +1,6 @@
 // TREDUCE / reduce_scatter / allreduce kernels for __half elements (one translation unit
 // per element type so the library builds in parallel).
-#include "reduce_impl.cuh"
+#include "reduce_forms.cuh"
 
 namespace ptoc {
 
