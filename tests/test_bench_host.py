@@ -1,8 +1,9 @@
 """Host-side logic of the multi-GPU benchmark, on CPU: world-size-2 gloo ranks
 run bench.aggregate (max step time over ranks, whole-job value) and fail with an
 error, not a hang, when one rank leaves before the exchange; the argument
-parser keeps the driver's defaults, and the reference arm's JSON line has the
-keys the contract asks for."""
+parser keeps its documented defaults (one GPU, at least three warm-up steps,
+the 16384 x 8192 TREDUCE case), and the reference arm's JSON line has the keys
+of the benchmark line."""
 import json
 import os
 import socket
