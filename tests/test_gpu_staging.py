@@ -160,3 +160,18 @@ def test_waits_that_run_out_are_counted_and_recovered(kind, monkeypatch):
     assert P.ptoc_wait_faults() == 0
     got = to_host(dst, np.float32)
     assert np.array_equal(bits(got), bits(want)), first_diff(got, want)
+
+
+def test_allreduce_f16_n8_8192x4096_full(form):
+    """8 windows fp16 [8192, 4096], N(0, 1), Sum, fused allreduce in the form
+    under test (the tensor setting runs the register form here): every
+    element of every window against the oracle."""
+    cfg = synth.WINDOWS_F16_N8_8192X4096
+    n, rows, cols, ld = cfg["nranks"], cfg["rows"], cfg["cols"], cfg["ld"]
+    host = [synth.window(r) for r in range(n)]
+    dev = [to_dev(h) for h in host]
+    P.ptoc_allreduce(dev, rows, cols, ld, P.SUM, P.F16)
+    assert oracle.allreduce(host, rows, cols, ld, oracle.SUM, oracle.F16) == 0
+    for r in range(n):
+        got = to_host(dev[r], np.uint16)
+        assert np.array_equal(got, host[r]), "window %d: %s" % (r, first_diff(got, host[r]))
