@@ -93,3 +93,21 @@ def oracle_treduce_threaded(srcs, dst, valid_rows, valid_cols, ld, op, dtype, th
     with ThreadPoolExecutor(threads) as ex:
         rcs = list(ex.map(part, range(threads)))
     return next((rc for rc in rcs if rc != 0), 0)
+
+
+def oracle_allreduce_threaded(windows, rows, cols, ld, op, dtype, threads=None):
+    """oracle.allreduce over contiguous row slices of every window, one host
+    thread each (allreduce acts row by row, so the split run writes exactly
+    what one call writes; checked on the CPU in test_oracle_split.py)."""
+    threads = threads or os.cpu_count() or 1
+    bounds = [rows * t // threads for t in range(threads + 1)]
+
+    def part(t):
+        a, b = bounds[t], bounds[t + 1]
+        if b <= a:
+            return 0
+        return oracle.allreduce([w[a:b] for w in windows], b - a, cols, ld, op, dtype)
+
+    with ThreadPoolExecutor(threads) as ex:
+        rcs = list(ex.map(part, range(threads)))
+    return next((rc for rc in rcs if rc != 0), 0)

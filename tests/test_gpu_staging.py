@@ -15,7 +15,8 @@ import torch
 import oracle
 import synth
 import tile_level_collective_gb300 as P
-from gpu_util import NP_STORE, ORC_DT, ORC_OP, bits, first_diff, oracle_treduce_threaded, to_dev, to_host
+from gpu_util import (NP_STORE, ORC_DT, ORC_OP, bits, first_diff, oracle_allreduce_threaded, oracle_treduce_threaded,
+                      to_dev, to_host)
 import test_gpu_collectives as coll
 import test_gpu_widen as widen
 from test_gpu_treduce import PCODE, SMALL, run_case
@@ -171,7 +172,7 @@ def test_allreduce_f16_n8_8192x4096_full(form):
     host = [synth.window(r) for r in range(n)]
     dev = [to_dev(h) for h in host]
     P.ptoc_allreduce(dev, rows, cols, ld, P.SUM, P.F16)
-    assert oracle.allreduce(host, rows, cols, ld, oracle.SUM, oracle.F16) == 0
+    assert oracle_allreduce_threaded(host, rows, cols, ld, oracle.SUM, oracle.F16) == 0
     for r in range(n):
         got = to_host(dev[r], np.uint16)
         assert np.array_equal(got, host[r]), "window %d: %s" % (r, first_diff(got, host[r]))

@@ -11,7 +11,7 @@ import torch
 import oracle
 import synth
 import tile_level_collective_gb300 as P
-from gpu_util import DevBuf, NP_STORE, ORC_DT, bits, first_diff, to_dev, to_host
+from gpu_util import DevBuf, NP_STORE, ORC_DT, bits, first_diff, oracle_allreduce_threaded, to_dev, to_host
 from test_gpu_collectives import windows_host
 from test_gpu_treduce import PCODE, nan_equal
 
@@ -173,7 +173,7 @@ def test_allreduce_full_size_f16():
     P.ptoc_allreduce(dev, rows, cols, ld, P.SUM, P.F16)
     P.ptoc_reduce_scatter(dev2, rows, cols, ld, P.SUM, P.F16)
     P.ptoc_allgather(dev2, rows, cols, ld, P.F16)
-    oracle.allreduce(host, rows, cols, ld, oracle.SUM, oracle.F16)
+    assert oracle_allreduce_threaded(host, rows, cols, ld, oracle.SUM, oracle.F16) == 0
     for r in range(n):
         got = to_host(dev[r], np.uint16)
         assert np.array_equal(got, host[r]), "window %d: %s" % (r, first_diff(got, host[r]))
