@@ -107,9 +107,10 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint64
 // their way while the other warps arrive); every thread with a vector then
 // waits for rank 0's copy, initialises its accumulator, and folds ranks
 // 1..n-1 as their copies land, in rank order; the stores are those of the
-// register form. A wait that gives up (it never does on valid memory) adds 1
-// to g_stage_faults, and the block waits once more, bounded, for its copies
-// in flight and returns without storing that tile or any later one.
+// register form. A wait that gives up (with the default bound it never does
+// on valid memory) adds 1 to g_stage_faults, and the block waits once more,
+// with the full bound, for its copies in flight and returns without storing
+// that tile or any later one.
 template <class T, int OP>
 __global__ void __launch_bounds__(kBlock) reduce_staged_kernel(const __grid_constant__ ReduceParams p)
 {
