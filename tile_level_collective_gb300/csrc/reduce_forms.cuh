@@ -100,6 +100,37 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint64
     return false;
 }
 
+// The fold of one staged tile for the calling thread: its 16 bytes of rank
+// r's segment sit at `mine` + r * kBlock * 16 in shared memory, and rank r's
+// copy completes on bars[r]. Waits for the ranks in order (each bounded by
+// the launch's bound), folding each as it lands; false if a wait gave up.
+template <class T, int OP>
+__device__ __forceinline__ bool fold_staged(const uint64_t* bars, int n, uint32_t parity, uint32_t mine,
+                                            uint64_t bound_ns, Words<4>& out)
+{
+    const uint64_t deadline = globaltimer_ns() + bound_ns;
+    VecAcc<T, OP, 4> acc;
+    if (!stage_wait(smem_u32(&bars[0]), parity, deadline, bound_ns)) return false;
+    acc.init(stage_load(mine));
+    for (int r = 1; r < n; ++r) {
+        if (!stage_wait(smem_u32(&bars[r]), parity, deadline, bound_ns)) return false;
+        acc.add(stage_load(mine + (uint32_t)(r * kBlock * 16)));
+    }
+    out = acc.out();
+    return true;
+}
+
+// A block one of whose waits gave up: count the fault, wait (with the full
+// bound) for each rank's copy still in flight, so that no copy lands in shared
+// memory the block no longer owns, and meet the block before it returns.
+__device__ __forceinline__ void give_up_tile(const uint64_t* bars, int n, uint32_t parity)
+{
+    if (threadIdx.x == 0) atomicAdd(&g_stage_faults, 1u);
+    if ((int)threadIdx.x < n)
+        stage_wait(smem_u32(&bars[threadIdx.x]), parity, globaltimer_ns() + kStageWaitNs, kStageWaitNs);
+    __syncthreads();
+}
+
 // Tiles as in reduce_kernel (one row segment of kBlock 16-byte vectors), the
 // sources staged in dynamic shared memory: rank r's segment at r * kBlock
 // vectors. Thread r < n owns rank r's mbarrier and starts that rank's copy
@@ -163,22 +194,13 @@ __global__ void __launch_bounds__(kBlock) reduce_staged_kernel(const __grid_cons
         issued = false;
         bool ok = true;
         if (tid < nv) {
-            const uint64_t deadline = globaltimer_ns() + p.wait_ns;
-            const uint32_t mine = smem_u32(stage + tid);
-            VecAcc<T, OP, 4> acc;
-            ok = stage_wait(smem_u32(&bars[0]), parity, deadline, p.wait_ns);
-            if (ok) acc.init(stage_load(mine));
-            for (int r = 1; r < n && ok; ++r) {
-                ok = stage_wait(smem_u32(&bars[r]), parity, deadline, p.wait_ns);
-                if (ok) acc.add(stage_load(mine + (uint32_t)(r * kBlock * 16)));
-            }
-            if (ok) store_result<4>(p, row, off0 + (int64_t)tid * 16, acc.out());
+            Words<4> v;
+            ok = fold_staged<T, OP>(bars, n, parity, smem_u32(stage + tid), p.wait_ns, v);
+            if (ok) store_result<4>(p, row, off0 + (int64_t)tid * 16, v);
         }
         // every thread is done with the stage before it is refilled
         if (!__syncthreads_and(ok)) {
-            if (tid == 0) atomicAdd(&g_stage_faults, 1u);
-            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs, kStageWaitNs);
-            __syncthreads();
+            give_up_tile(bars, n, parity);
             return;
         }
         parity ^= 1u;
@@ -257,28 +279,18 @@ __global__ void __launch_bounds__(kBlock) reduce_tma2d_kernel(const __grid_const
             issue(w);
         }
         first = false;
-        const uint64_t deadline = globaltimer_ns() + p.wait_ns;
         const uint32_t mine = smem_u32(stage + tid);
-        VecAcc<T, OP, 4> acc;
-        bool ok = stage_wait(smem_u32(&bars[0]), parity, deadline, p.wait_ns);
-        if (ok) acc.init(stage_load(mine));
-        for (int r = 1; r < n && ok; ++r) {
-            ok = stage_wait(smem_u32(&bars[r]), parity, deadline, p.wait_ns);
-            if (ok) acc.add(stage_load(mine + (uint32_t)(r * kBlock * 16)));
-        }
-        if (ok) {
-            const Words<4> v = acc.out();
+        Words<4> v;
+        const bool ok = fold_staged<T, OP>(bars, n, parity, mine, p.wait_ns, v);
+        if (ok)
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
                          ::"r"(mine), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
                          : "memory");
-        }
         // the result box is complete (and visible to the async proxy) before
         // thread 0 stores it; a failed wait anywhere skips the store
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (!__syncthreads_and(ok)) {
-            if (tid == 0) atomicAdd(&g_stage_faults, 1u);
-            if (tid < n) stage_wait(smem_u32(&bars[tid]), parity, globaltimer_ns() + kStageWaitNs, kStageWaitNs);
-            __syncthreads();
+            give_up_tile(bars, n, parity);
             return;
         }
         if (tid == 0)
