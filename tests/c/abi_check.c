@@ -1,10 +1,12 @@
 /*
  * A plain C caller of libptoc.so: allocates its own buffers with the CUDA
  * runtime, runs TREDUCE (Sum, Max, Min) over ranks holding base + 100 r (the
- * TREDUCE article's own test, section 7.1) and an all_to_all_v with clamped
- * counts, and checks the results against the closed forms. Exit status 0 when
- * everything matches; the first mismatch is printed.
+ * TREDUCE article's own test, section 7.1), in the register form and in the
+ * staged form (PTOC_REDUCE_STAGING), and an all_to_all_v with clamped counts,
+ * checks the results against the closed forms, and reads the wait-fault
+ * count. Exit status 0 when everything matches; the first mismatch is printed.
  */
+#define _POSIX_C_SOURCE 200112L
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -40,7 +42,10 @@ int main(void)
     if (cudaMalloc(&dst, bytes) != cudaSuccess) return 2;
     ptoc_group g = {src, N, 0};
     const ptoc_reduce_op ops[3] = {PTOC_SUM, PTOC_MAX, PTOC_MIN};
-    for (int o = 0; o < 3; ++o) {
+    const char* forms[2] = {"regs", "bulk"};
+    for (int f = 0; f < 6; ++f) {
+        const int o = f % 3;
+        setenv("PTOC_REDUCE_STAGING", forms[f / 3], 1);
         cudaMemset(dst, 0xFF, bytes);
         ptoc_status st = ptoc_treduce(&g, dst, ROWS, COLS, ROWS, COLS, LD, ops[o], PTOC_I32, 0);
         if (st != PTOC_OK) {
@@ -57,6 +62,9 @@ int main(void)
                 if (host[i * LD + j] != want) return fail("treduce", i * LD + j, host[i * LD + j], want);
             }
     }
+    unsetenv("PTOC_REDUCE_STAGING");
+    uint32_t faults = 1;
+    if (ptoc_wait_faults(&faults) != PTOC_OK || faults != 0) return fail("wait faults", 0, (long)faults, 0);
     /* bad arguments come back as status codes, nothing launched */
     if (ptoc_treduce(&g, dst, ROWS, COLS, ROWS, COLS, LD, PTOC_PROD, PTOC_I32, 0) != PTOC_ERR_UNSUPPORTED)
         return fail("prod status", 0, 0, PTOC_ERR_UNSUPPORTED);
