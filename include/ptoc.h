@@ -85,6 +85,12 @@
  *                        least 1.5 GiB (N reads plus the writes), "regs"
  *                        below, the faster form at each size on GB300.
  *                        Results are identical in every form.
+ *   PTOC_L2_PREFETCH=0   turn off the first-wave L2 prefetch of the register
+ *                        form: by default, in a reduction that moves less than
+ *                        512 MiB, each block of the first wave (8 per SM) asks
+ *                        L2 for its first tile before it waits for the previous
+ *                        kernel of the stream, so that back-to-back calls keep
+ *                        DRAM busy across the boundary between them.
  *   PTOC_WAIT_NS=<ns>    the bound on one wait of the staged and tensor forms
  *                        for a copy to land (1 ns to 60 s; default 2 s). A
  *                        block whose wait runs out stores nothing more,

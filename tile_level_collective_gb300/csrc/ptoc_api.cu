@@ -49,6 +49,18 @@ bool staged_reduction(int64_t bytes)
     return bytes >= kStagedMinBytes;
 }
 
+namespace {
+int sm_count();
+}
+
+int32_t first_wave_prefetch(int64_t bytes)
+{
+    constexpr int64_t kPrefetchBelowBytes = (int64_t)512 << 20;
+    const char* e = getenv("PTOC_L2_PREFETCH");
+    if ((e && strcmp(e, "0") == 0) || bytes >= kPrefetchBelowBytes) return 0;
+    return 8 * sm_count();
+}
+
 uint64_t copy_wait_ns()
 {
     const uint64_t dflt = 2000000000ull, most = 60000000000ull;
@@ -339,7 +351,9 @@ cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, i
     // every window for allreduce)
     const int64_t writes = p.dst_mode == kDstAll ? p.nranks : 1;
     const int64_t elems = rows > 0 && cols > 0 ? rows * cols : 0;
-    p.staged = staged_reduction((p.nranks + writes) * eb * elems) ? 1 : 0;
+    const int64_t bytes = (p.nranks + writes) * eb * elems;
+    p.staged = staged_reduction(bytes) ? 1 : 0;
+    p.prefetch_blocks = p.staged ? 0 : first_wave_prefetch(bytes);
     p.wait_ns = copy_wait_ns();
     return launch_reduce_regs(dtype, p, op, vb, grid_for(p.ntiles + p.tail_blocks), s);
 }

@@ -38,6 +38,7 @@ struct ReduceParams {
     int32_t nranks;
     int32_t dst_mode;             // DstMode
     int32_t staged;               // 1: the staged form where it applies (host-side choice)
+    int32_t prefetch_blocks;      // blocks below this prefetch their first tile into L2 (register form)
     uint64_t wait_ns;             // the staged form's bound on one wait for a copy
 };
 
@@ -122,6 +123,13 @@ cudaError_t launch_credit_barrier(const BarrierParams& p, cudaStream_t s);
 // be visible) before touching memory. On by default; the documented switch
 // PTOC_PDL=0 turns it off.
 bool programmatic_launch();
+
+// How many of a register-form reduction's first blocks prefetch their first
+// tile into L2 before waiting for the previous kernel of the stream: the
+// first wave (8 blocks per SM) for launches that move less than 512 MiB,
+// none for larger ones or when the documented switch PTOC_L2_PREFETCH=0 is
+// set.
+int32_t first_wave_prefetch(int64_t bytes);
 
 // Whether a reduction that moves `bytes` per launch takes the staged form
 // (sources copied into shared memory by the bulk-copy engine) where it

@@ -543,9 +543,34 @@ __device__ __forceinline__ void reduce_tail_block(const ReduceParams& p, int64_t
 // normally has one block per work item, so the hardware block scheduler hands
 // out the tiles in order as blocks retire; a grid-stride loop covers grids
 // capped below the item count.
+// Before it waits for the previous kernel of the stream, a block of the first
+// wave asks L2 for its first tile (one bulk prefetch per rank, on 16-byte
+// vectors): a programmatic dependent launch starts these blocks while the
+// previous kernel's last blocks still run, and the prefetch lets DRAM fetch
+// the tile meanwhile. A prefetch returns no data, and L2 is where every write
+// to device memory lands, so the loads after the wait still see the previous
+// kernel's writes.
+template <class T, int VB>
+__device__ __forceinline__ void prefetch_first_tile(const ReduceParams& p)
+{
+    if constexpr (VB == 16) {
+        if (blockIdx.x < (unsigned)p.prefetch_blocks && blockIdx.x < p.ntiles && (int)threadIdx.x < p.nranks) {
+            const int64_t row = blockIdx.x / p.tpr;
+            const int64_t v0 = (blockIdx.x - row * p.tpr) * kBlock;
+            const int64_t nv = p.vpr - v0 < kBlock ? p.vpr - v0 : kBlock;
+            if (nv > 0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             ::"l"((const char*)p.src[threadIdx.x] + row * p.ld * (int64_t)sizeof(T) + v0 * 16),
+                               "r"((uint32_t)(nv * 16))
+                             : "memory");
+        }
+    }
+}
+
 template <class T, int OP, int VB, int FORM>
 __global__ void __launch_bounds__(kBlock) reduce_kernel(const __grid_constant__ ReduceParams p)
 {
+    prefetch_first_tile<T, VB>(p);
     pdl_enter();
     const int64_t total = p.ntiles + p.tail_blocks;
     for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
