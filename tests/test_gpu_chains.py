@@ -64,3 +64,38 @@ def test_dependent_chain(pdl, monkeypatch):
         oracle.all_to_all_v_combine(ot, oo, orc_, tr, size, oracle.ATOMIC_ADD, oracle.I32)
         for t, o in zip(outs, oo):
             assert np.array_equal(to_host(t, np.int32), o)
+
+
+@pytest.mark.parametrize("prefetch", ["1", "0"])
+def test_first_wave_prefetch_of_rows_written_last(prefetch, monkeypatch):
+    """The register form's first wave asks L2 for its first tiles before it
+    waits for the previous kernel. Here the next call's sources are the rows
+    the previous call writes in its last waves (the tail of a 64 MiB result),
+    and every iteration writes new values there, so a prefetch that served a
+    stale line would show. Bit for bit against the oracle, prefetch on and
+    off, programmatic dependent launch on."""
+    monkeypatch.setenv("PTOC_PDL", "1")
+    monkeypatch.setenv("PTOC_L2_PREFETCH", prefetch)
+    n, rows, cols, tail = 4, 4096, 4096, 256
+    rng = np.random.default_rng(9)
+    hs = [rng.integers(-(1 << 28), 1 << 28, size=(rows, cols)).astype(np.int32) for _ in range(n)]
+    srcs = [to_dev(h) for h in hs]
+    d1 = torch.empty(rows, cols, dtype=torch.int32, device="cuda")
+    d2 = torch.empty(tail, cols, dtype=torch.int32, device="cuda")
+    d3 = torch.empty_like(d2)
+    d1_tail = d1[rows - tail:]
+    for it in range(6):
+        a, b = it % n, (it + 1) % n
+        P.ptoc_treduce([srcs[a], srcs[b]], d1, rows, cols, rows, cols, cols, P.SUM, P.I32)
+        P.ptoc_treduce([d1_tail, srcs[2][:tail]], d2, tail, cols, tail, cols, cols, P.MAX, P.I32)
+        P.ptoc_treduce([d2, d1_tail], d3, tail, cols, tail, cols, cols, P.SUM, P.I32)
+        torch.cuda.synchronize()
+        o1 = np.zeros((tail, cols), np.int32)
+        oracle.treduce([hs[a][rows - tail:], hs[b][rows - tail:]], o1, tail, cols, cols, oracle.SUM, oracle.I32)
+        o2 = np.zeros_like(o1)
+        oracle.treduce([o1, hs[2][:tail]], o2, tail, cols, cols, oracle.MAX, oracle.I32)
+        o3 = np.zeros_like(o1)
+        oracle.treduce([o2, o1], o3, tail, cols, cols, oracle.SUM, oracle.I32)
+        assert np.array_equal(to_host(d1_tail, np.int32), o1), "iteration %d: d1 tail" % it
+        assert np.array_equal(to_host(d2, np.int32), o2), "iteration %d: d2" % it
+        assert np.array_equal(to_host(d3, np.int32), o3), "iteration %d: d3" % it
