@@ -1437,10 +1437,11 @@ def run_ours(args):
         e_ms, e_value = None, None
     else:
         e_ms, e_value = run_e2e(wl, args, dev, stream, world, barrier)
+    link = host_link_gbs(dev) if e_value is not None and rank == 0 else None
     if rank != 0:
         return
     line = build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl,
-                      sampler.summary(t0, t1) if sampler else None, len(blocks), block_gbs, t1 - t0)
+                      sampler.summary(t0, t1) if sampler else None, len(blocks), block_gbs, t1 - t0, link)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -1503,14 +1504,51 @@ def run_e2e(wl, args, dev, stream, world, barrier):
     return run_e2e_pipelined(wl, args, dev, world, barrier)
 
 
+def host_link_gbs(dev, nbytes=256 << 20, reps=5):
+    """Pinned host <-> device copy rates on this machine (GB/s, best of `reps`
+    copies of `nbytes` each way, timed with events on a stream of their own):
+    the bound the e2e leg is compared against."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+    rates = []
+    for up in (True, False):
+        best = None
+        with torch.cuda.stream(s):
+            for _ in range(reps + 1):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                (d.copy_(h, non_blocking=True) if up else h.copy_(d, non_blocking=True))
+                b.record(s)
+                b.synchronize()
+                ms = a.elapsed_time(b)
+                best = ms if best is None else min(best, ms)
+        rates.append(nbytes / (best / 1e3) / 1e9)
+    del h, d
+    return rates[0], rates[1]
+
+
 def line_config(wl, world):
     """The `config` of both arms' lines (identical for the same workload and
     rank count)."""
     return dict(wl.config(), parallelism="replicas" if world > 1 else "single GPU")
 
 
+def e2e_link_bound(wl, link, world):
+    """The e2e leg's bound on this machine: every byte of a step crosses the
+    host link, uploads and downloads each at their measured rate and never
+    slowing each other (an optimistic bound: measured together, both ran
+    about a fifth slower)."""
+    up, down = link
+    t = max(wl.h2d_bytes() / (up * 1e9), wl.d2h_bytes() / (down * 1e9))
+    return {"h2d_gbs": round(up, 1), "d2h_gbs": round(down, 1),
+            "bound_gbs": round(wl.bytes_per_step() * world / t / 1e9, 2) if t > 0 else None,
+            "measured": "pinned 256 MiB copies each way on this GPU, best of 5, after the e2e leg"}
+
+
 def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl, clocks,
-               nblocks=1, block_gbs=None, timed_s=None):
+               nblocks=1, block_gbs=None, timed_s=None, link=None):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
@@ -1527,7 +1565,8 @@ def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traff
             "path": ("every step: pinned host -> device copy of its inputs, the library calls, device -> "
                      "pinned host copy of its results; double-buffered on three streams (upload of step k "
                      "overlaps compute and download of step k-1); the last results checked against the "
-                     "resident run")},
+                     "resident run"),
+            "link": e2e_link_bound(wl, link, world) if link else None},
         "gpu_launches": nl * args.steps * nblocks,
         "timing": ("CUDA events around each launch" if wl.per_launch_timing else
                    "CUDA events around each step; its %d launches run back to back (programmatic "

@@ -304,3 +304,25 @@ def test_reference_arm_runs_on_rank_zero_only():
                          capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == ""
+
+
+def test_e2e_link_bound():
+    """The e2e leg's bound: the slower direction of the host link sets the
+    step time, the step's bytes over that time is the bound, whole job."""
+    import bench
+
+    class W:
+        def h2d_bytes(self):
+            return 8 * 10 ** 9
+
+        def d2h_bytes(self):
+            return 1 * 10 ** 9
+
+        def bytes_per_step(self):
+            return 9 * 10 ** 9
+
+    b = bench.e2e_link_bound(W(), (200.0, 100.0), 1)
+    assert b["h2d_gbs"] == 200.0 and b["d2h_gbs"] == 100.0
+    assert b["bound_gbs"] == pytest.approx(9e9 / 0.04 / 1e9)        # upload: 40 ms against 10 ms down
+    b = bench.e2e_link_bound(W(), (200.0, 10.0), 2)
+    assert b["bound_gbs"] == pytest.approx(2 * 9e9 / 0.1 / 1e9)      # download: 100 ms
