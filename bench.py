@@ -1434,10 +1434,10 @@ def run_ours(args):
 
     # end to end: pinned host inputs in, results out, every step
     if args.no_e2e:
-        e_ms, e_value = None, None
+        e_ms, e_value, e_up = None, None, None
     else:
-        e_ms, e_value = run_e2e(wl, args, dev, stream, world, barrier)
-    link = host_link_gbs(dev) if e_value is not None and rank == 0 else None
+        e_ms, e_value, e_up = run_e2e(wl, args, dev, stream, world, barrier)
+    link = host_link_gbs(dev) + (e_up,) if e_value is not None and rank == 0 else None
     if rank != 0:
         return
     line = build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl,
@@ -1459,8 +1459,9 @@ def run_e2e_pipelined(wl, args, dev, world, barrier):
     ev = lambda: torch.cuda.Event()
     uploaded, computed, downloaded = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     used = [False, False]
+    upload_events = []
 
-    def run(steps):
+    def run(steps, timed=False):
         for k in range(steps):
             b = k & 1
             with torch.cuda.stream(up):
@@ -1468,7 +1469,12 @@ def run_e2e_pipelined(wl, args, dev, world, barrier):
                     # the set's inputs are free once computed; in place, its
                     # results must also have been read back
                     up.wait_event(downloaded[b] if wl.e2e_inplace else computed[b])
+                if timed:
+                    upload_events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                    upload_events[-1][0].record(up)
                 wl.e2e_upload(b)
+                if timed:
+                    upload_events[-1][1].record(up)
                 uploaded[b].record(up)
             with torch.cuda.stream(comp):
                 comp.wait_event(uploaded[b])
@@ -1489,13 +1495,16 @@ def run_e2e_pipelined(wl, args, dev, world, barrier):
     barrier()
     torch.cuda.synchronize()
     es.record(up)
-    run(e_steps)
+    run(e_steps, timed=True)
     down.wait_stream(up)
     down.wait_stream(comp)
     ee.record(down)
     torch.cuda.synchronize()
     wl.e2e_verify((e_steps - 1) & 1)
-    return aggregate(es.elapsed_time(ee) / e_steps, wl.bytes_per_step(), world, dev)
+    up_ms = sum(a.elapsed_time(b) for a, b in upload_events)
+    upload_gbs = wl.h2d_bytes() * len(upload_events) / (up_ms / 1e3) / 1e9 if up_ms > 0 else None
+    e_ms, e_value = aggregate(es.elapsed_time(ee) / e_steps, wl.bytes_per_step(), world, dev)
+    return e_ms, e_value, upload_gbs
 
 
 def run_e2e(wl, args, dev, stream, world, barrier):
@@ -1535,16 +1544,19 @@ def line_config(wl, world):
     return dict(wl.config(), parallelism="replicas" if world > 1 else "single GPU")
 
 
-def e2e_link_bound(wl, link, world):
+def e2e_link_bound(wl, link, world, during=None):
     """The e2e leg's bound on this machine: every byte of a step crosses the
     host link, uploads and downloads each at their measured rate and never
     slowing each other (an optimistic bound: measured together, both ran
-    about a fifth slower)."""
+    about a fifth slower). `during` is the upload rate the e2e leg itself
+    saw (its uploads timed on their stream), which other traffic on the
+    host side can hold below the probe's."""
     up, down = link
     t = max(wl.h2d_bytes() / (up * 1e9), wl.d2h_bytes() / (down * 1e9))
     return {"h2d_gbs": round(up, 1), "d2h_gbs": round(down, 1),
             "bound_gbs": round(wl.bytes_per_step() * world / t / 1e9, 2) if t > 0 else None,
-            "measured": "pinned 256 MiB copies each way on this GPU, best of 5, after the e2e leg"}
+            "measured": "pinned 256 MiB copies each way on this GPU, best of 5, after the e2e leg",
+            "h2d_gbs_during_e2e": round(during, 1) if during else None}
 
 
 def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traffic, e_value, e_ms, nl, clocks,
@@ -1566,7 +1578,7 @@ def build_line(args, wl, world, value, ms, achieved, avg0, peak, peak_src, traff
                      "pinned host copy of its results; double-buffered on three streams (upload of step k "
                      "overlaps compute and download of step k-1); the last results checked against the "
                      "resident run"),
-            "link": e2e_link_bound(wl, link, world) if link else None},
+            "link": e2e_link_bound(wl, link[:2], world, link[2]) if link else None},
         "gpu_launches": nl * args.steps * nblocks,
         "timing": ("CUDA events around each launch" if wl.per_launch_timing else
                    "CUDA events around each step; its %d launches run back to back (programmatic "

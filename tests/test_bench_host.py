@@ -324,5 +324,7 @@ def test_e2e_link_bound():
     b = bench.e2e_link_bound(W(), (200.0, 100.0), 1)
     assert b["h2d_gbs"] == 200.0 and b["d2h_gbs"] == 100.0
     assert b["bound_gbs"] == pytest.approx(9e9 / 0.04 / 1e9)        # upload: 40 ms against 10 ms down
-    b = bench.e2e_link_bound(W(), (200.0, 10.0), 2)
+    assert b["h2d_gbs_during_e2e"] is None
+    b = bench.e2e_link_bound(W(), (200.0, 10.0), 2, during=150.04)
     assert b["bound_gbs"] == pytest.approx(2 * 9e9 / 0.1 / 1e9)      # download: 100 ms
+    assert b["h2d_gbs_during_e2e"] == 150.0
