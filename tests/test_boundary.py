@@ -211,3 +211,18 @@ def test_device_count_exchanges_reject_int32_tile_overflow():
                                        check=False) == P.ERR_UNSUPPORTED
     assert P.ptoc_all_to_all_v_combine(ins, tgs, rc, tr_, size, P.ATOMIC_ADD, P.BF16, stream=0,
                                        check=False) == P.ERR_UNSUPPORTED
+
+
+def test_package_refuses_to_import_without_the_library(tmp_path):
+    """No fallback path: a copy of the binding without libptoc.so beside it
+    raises ImportError at import, naming the missing library."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "tile_level_collective_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(ROOT, "tile_level_collective_gb300", "__init__.py"), pkg / "__init__.py")
+    r = subprocess.run([sys.executable, "-c", "import tile_level_collective_gb300"], cwd=tmp_path,
+                       capture_output=True, text=True, env=dict(os.environ, PYTHONPATH=str(tmp_path)))
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libptoc.so is not built" in r.stderr
