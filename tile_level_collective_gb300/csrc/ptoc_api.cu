@@ -351,7 +351,8 @@ cudaError_t launch_reduction(int dtype, ReduceParams& p, int op, int64_t rows, i
     // every window for allreduce)
     const int64_t writes = p.dst_mode == kDstAll ? p.nranks : 1;
     const int64_t elems = rows > 0 && cols > 0 ? rows * cols : 0;
-    const int64_t bytes = (p.nranks + writes) * eb * elems;
+    const int64_t per_elem = (p.nranks + writes) * eb;
+    const int64_t bytes = elems > INT64_MAX / per_elem ? INT64_MAX : per_elem * elems;
     p.staged = staged_reduction(bytes) ? 1 : 0;
     p.prefetch_blocks = p.staged ? 0 : first_wave_prefetch(bytes);
     p.wait_ns = copy_wait_ns();
