@@ -54,6 +54,9 @@ __device__ __forceinline__ To bitcast(const From& f)
 }
 
 // ---- vector loads and stores (L1 bypass: every byte is touched once) -------
+// The loads are volatile and clobber memory, like the stores and the wait of
+// a programmatic dependent launch: the compiler keeps every load after that
+// wait, so no load can read a source before the previous kernel's writes.
 
 template <int W>
 __device__ __forceinline__ Words<W> load_words(const char* p);
@@ -62,22 +65,22 @@ template <>
 __device__ __forceinline__ Words<4> load_words<4>(const char* p)
 {
     Words<4> r;
-    asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "l"(p));
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "l"(p) : "memory");
     return r;
 }
 template <>
 __device__ __forceinline__ Words<2> load_words<2>(const char* p)
 {
     Words<2> r;
-    asm("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p));
+    asm volatile("ld.global.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "l"(p) : "memory");
     return r;
 }
 template <>
 __device__ __forceinline__ Words<1> load_words<1>(const char* p)
 {
     Words<1> r;
-    asm("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(r.w[0]) : "l"(p));
+    asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(r.w[0]) : "l"(p) : "memory");
     return r;
 }
 
@@ -118,7 +121,7 @@ struct Chunk<2> {
     static __device__ __forceinline__ type load(const char* p)
     {
         Elem16 r;
-        asm("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(r.h) : "l"(p));
+        asm volatile("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(r.h) : "l"(p) : "memory");
         return r;
     }
     static __device__ __forceinline__ void store(char* p, const type& v)
